@@ -1,0 +1,203 @@
+/*
+ * precision_gemm.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * The operation is dense single-precision matrix multiply,
+ *
+ *     C = alpha * op(A) * op(B) + beta * C,
+ *
+ * on column-major storage with leading dimensions.  Sources for this contract:
+ *   - "Optimizing SGEMM on NVIDIA Turing GPUs" (README): SGEMM with column-major
+ *     A and B, not transposed, is the primary case.
+ *   - "HPC - Lecture 13 - MatMat GPU", sections "Kernel 1: Global Memory Access"
+ *     and "function matmatgpu1": the product accumulates into C (C += A*B), and
+ *     the host routine takes strided arrays with leading dimensions lda, ldb,
+ *     ldc, moves them to the device, launches, and copies C back.
+ *   - "V3. Vectorized and double buffer" (Explore-GPU-performance wiki),
+ *     section 2: a row-major kernel that overwrites C; row-major storage is
+ *     the column-major storage of the transpose, so it needs no entry of its
+ *     own (C^T = B^T * A^T, with the operands and m/n swapped).
+ *
+ * Conventions shared by every call below:
+ *   - Element (i, j) of a stored matrix X with leading dimension ldx is
+ *     X[i + j*ldx].  op(A) is m x k, op(B) is k x n, C is m x n.
+ *   - trans is one of 'N','n' (op(X) = X) or 'T','t','C','c' (op(X) = X^T).
+ *   - The library reads A, B and C only inside their logical extents and writes
+ *     only C[i + j*ldc] for i < m, j < n; the leading-dimension gaps are never
+ *     touched.  When beta == 0 C is not read (NaN there does not propagate);
+ *     when alpha == 0 or k == 0, A and B are not read.
+ *   - Return value: 0 on success; -i when the i-th argument (1-based, in the
+ *     order of the signature) is invalid, checked in signature order and before
+ *     any device work; a positive SGEMM_ERR_* code for device-side failures.
+ *     sgemm_last_error_string() describes the last failure on the calling
+ *     thread.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream) unless stated otherwise.
+ *   - A failure detected inside a running kernel (a bounded wait that
+ *     expired) cannot be returned by the launching call; it is recorded in a
+ *     per-device status word that sgemm_device_status() reads.
+ */
+#ifndef PRECISION_GEMM_H
+#define PRECISION_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Arithmetic modes (argument `mode`). */
+#define SGEMM_FFMA 0   /* exact FP32 fused multiply-add on the CUDA cores          */
+#define SGEMM_TF32 1   /* tensor cores (tcgen05), TF32 inputs, FP32 accumulation  */
+#define SGEMM_3XTF32 2 /* tensor cores, each operand split x = big + small (both
+                          TF32); small*big + big*small + big*big accumulated in
+                          FP32, which recovers FP32-level accuracy               */
+
+/* Status codes. */
+#define SGEMM_SUCCESS 0
+#define SGEMM_ERR_CUDA 1       /* a CUDA runtime call or launch failed          */
+#define SGEMM_ERR_NO_DEVICE 2  /* no CUDA device is usable                      */
+#define SGEMM_ERR_ARCH 3       /* the current device is not compute capability 10.3 */
+#define SGEMM_ERR_TIMEOUT 4    /* a bounded in-kernel wait expired              */
+#define SGEMM_ERR_ALLOC 5      /* device or host allocation failed              */
+#define SGEMM_ERR_TENSOR_MAP 6 /* a TMA tensor map could not be encoded         */
+#define SGEMM_ERR_CAPTURE 7    /* workspace must grow while the stream is being
+                                  captured into a CUDA graph                    */
+
+/* Kernel families reported by sgemm_plan(). */
+#define SGEMM_KERNEL_NONE 0    /* nothing to do (m == 0, n == 0, or C unchanged) */
+#define SGEMM_KERNEL_SCALE 1   /* C = beta * C only (k == 0 or alpha == 0)       */
+#define SGEMM_KERNEL_FFMA 2    /* CUDA-core FP32 kernel                         */
+#define SGEMM_KERNEL_TC 3      /* tcgen05 tensor-core kernel                    */
+
+/* How an operand reaches the GEMM kernel (sgemm_plan_t.prep_a / prep_b). */
+#define SGEMM_PREP_NONE 0      /* read in place through TMA                     */
+#define SGEMM_PREP_COPY 1      /* copied into the workspace with an aligned ld  */
+#define SGEMM_PREP_TRANSPOSE 2 /* copied transposed (trans = 'T')               */
+#define SGEMM_PREP_SPLIT 3     /* split into big/small TF32 parts (3xTF32)      */
+
+/*
+ * sgemm -- C = alpha*op(A)*op(B) + beta*C on device memory.
+ *
+ *   transa, transb  'N'/'n' or 'T'/'t'/'C'/'c' (arguments 1, 2)
+ *   m, n, k         sizes, >= 0 (arguments 3, 4, 5)
+ *   alpha           scalar (6)
+ *   A, lda          device pointer; m x k matrix (k x m if transa is 'T'),
+ *                   lda >= max(1, rows of the stored matrix) (7, 8)
+ *   B, ldb          device pointer; k x n matrix (n x k if transb is 'T'),
+ *                   ldb >= max(1, rows of the stored matrix) (9, 10)
+ *   beta            scalar (11)
+ *   C, ldc          device pointer; m x n, ldc >= max(1, m) (12, 13)
+ *   mode            SGEMM_FFMA, SGEMM_TF32 or SGEMM_3XTF32 (14)
+ *   stream          cudaStream_t as void*, or NULL (15)
+ *
+ * Ownership: the caller owns A, B and C and keeps them alive until the work
+ * on `stream` completes.  The library owns a workspace per (device, stream)
+ * for operand copies, 3xTF32 split operands and split-K partial sums; it grows
+ * on demand with stream-ordered allocation and is released by
+ * sgemm_workspace_release().  Calls on the same stream are ordered; calls on
+ * different streams use different workspaces.  A null pointer is an invalid
+ * argument only when the call would read or write through it.
+ *
+ * Results are deterministic: the same inputs, mode and device give bitwise
+ * identical C on every run (split-K partial sums are added in a fixed order).
+ */
+int sgemm(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+          const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+          float *C, int64_t ldc, int mode, void *stream);
+
+/*
+ * sgemm_host -- the same operation on HOST arrays (the shape of the lecture's
+ * matmatgpu1: copy the operands in, run the product, copy C back).
+ *
+ * Arguments as sgemm, but A, B and C are host pointers (pinned memory gives
+ * the fastest copies; pageable memory works).  The call copies the logical
+ * extents of A, B and (when beta != 0) C into library-owned device buffers on
+ * `stream`, runs sgemm, copies the m x n result back into C (its ld gaps are
+ * not written), and synchronises `stream` before returning, so C is ready
+ * when it returns 0.
+ */
+int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+               const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+               float *C, int64_t ldc, int mode, void *stream);
+
+/* The choices sgemm would make for a call (see sgemm_plan). */
+typedef struct sgemm_plan {
+    int kernel;              /* SGEMM_KERNEL_*                                  */
+    int mode;                /* the mode argument                               */
+    int bm, bn, bk, stages;  /* CTA tile and shared-memory ring depth           */
+    int split_k;             /* number of K slices (1: no split)                */
+    int k_blocks;            /* BK-sized blocks of K in total                   */
+    int k_blocks_per_split;  /* BK-sized blocks each slice reduces              */
+    int tiles_m, tiles_n;    /* output tiles                                    */
+    int prep_a, prep_b;      /* SGEMM_PREP_* per operand                        */
+    int threads;             /* threads per CTA of the GEMM kernel              */
+    int ctas_per_sm;         /* CTAs the kernel is built to co-schedule per SM  */
+    int64_t ld_a, ld_b;      /* leading dimension the kernel reads A and B with */
+    size_t smem_bytes;       /* dynamic shared memory of the GEMM kernel        */
+    size_t workspace_bytes;  /* device workspace the call needs                 */
+    int launches;            /* kernels the call launches                       */
+} sgemm_plan_t;
+
+/*
+ * sgemm_plan -- fill *plan with what sgemm would do for these arguments on a
+ * device with `num_sms` multiprocessors, without touching any device.
+ * The pointers are only inspected for alignment, never dereferenced, so this
+ * works on a machine without a GPU.  Returns 0, or -i for an invalid argument
+ * exactly as sgemm would (mode is argument 14, num_sms 15, plan 16).
+ */
+int sgemm_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+               const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
+               const void *C, int64_t ldc, int mode, int num_sms, sgemm_plan_t *plan);
+
+/*
+ * sgemm_device_status -- synchronise `stream`, then return SGEMM_SUCCESS, or
+ * SGEMM_ERR_TIMEOUT if any kernel of this library on the current device found
+ * a bounded wait expired since the status was last cleared, or SGEMM_ERR_CUDA
+ * if the synchronisation itself failed.  clear != 0 resets the status word.
+ */
+int sgemm_device_status(void *stream, int clear);
+
+/*
+ * sgemm_set_wait_timeout -- limit, in nanoseconds, of every in-kernel wait of
+ * kernels launched afterwards from any thread (default 4e9 = 4 s).  A kernel
+ * whose wait expires records SGEMM_ERR_TIMEOUT, waits (bounded) for its own
+ * copies in flight, frees its tensor memory and exits; its C is unspecified.
+ * Returns the previous limit.
+ */
+uint64_t sgemm_set_wait_timeout(uint64_t ns);
+
+/*
+ * sgemm_force_plan -- tuning override for later calls from any thread:
+ * bn in {0, 64, 128, 256} fixes the CTA tile width, split_k > 0 fixes the number
+ * of K slices (clamped to the number of K blocks).  0 restores the automatic
+ * choice.  Returns -1 for an unsupported bn, -2 for a negative split_k.
+ */
+int sgemm_force_plan(int bn, int split_k);
+
+/*
+ * sgemm_debug_flags -- test hook.  SGEMM_DEBUG_STALL_PRODUCER makes the
+ * operand loader of later GEMM kernels issue nothing, so the waits of the
+ * rest of the CTA expire (used by the failure-detection test); 0 clears.
+ * Returns the previous flags.
+ */
+#define SGEMM_DEBUG_STALL_PRODUCER 1
+int sgemm_debug_flags(int flags);
+
+/* Kernels this library has launched in this process (all devices). */
+uint64_t sgemm_launch_count(void);
+
+/* Free every cached workspace and staging buffer (synchronises the device). */
+int sgemm_workspace_release(void);
+
+/* Human-readable description of the last failure on the calling thread. */
+const char *sgemm_last_error_string(void);
+
+/* Library version string. */
+const char *sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRECISION_GEMM_H */

@@ -1,0 +1,270 @@
+// Exact-FP32 GEMM on the CUDA cores (FFMA), sm_103a.
+//
+// One CTA computes a 128 x BN tile of C from column-major A (m x k, M-major)
+// and B (k x n, K-major), both read through TMA.  Prior art on the pages --
+// register tiles of C per thread, shared-memory staging of A and B tiles,
+// float4 accesses and double buffering ("Optimizing SGEMM on NVIDIA Turing
+// GPUs", kernels 2-10; "V3. Vectorized and double buffer", sections 1-2) -- is
+// kept where it still holds on Blackwell and replaced where it does not:
+//
+//   * thread 0 issues TMA tile loads PD k-blocks ahead into a STAGES-deep ring
+//     of shared-memory slots, each guarded by a "full" mbarrier (TMA bytes
+//     landed) and an "empty" mbarrier (every warp is done with the slot); this
+//     replaces the pages' register prefetch + ping-pong buffers and their
+//     __syncthreads.  The loader is a consumer thread rather than a warp of its
+//     own so that the warps split evenly over the SM's four sub-partitions and
+//     each thread keeps 128 registers for its 8 x 8 tile;
+//   * the A tile lands as BK rows of 128 floats (k-major rows of m, the layout
+//     the wiki builds by hand with its transposed As[k][m] store); the B tile
+//     lands as BN rows of 32 floats (128 B) with the 128-byte TMA swizzle, so a
+//     quarter-warp reading one 16-byte chunk from 8 different rows hits 8
+//     different bank groups (no bank conflicts, the wiki's V3.1/V3.2 goal);
+//   * each consumer thread owns an 8 x 8 register tile: rows {4tm..4tm+3} and
+//     {64+4tm..64+4tm+3}, columns {tn + (BN/8)*jj}; per group of 4 k values it
+//     reads 8 float4 of B (4 k values of one column each) and 2 float4 of A per
+//     k, then issues 256 FMAs;
+//   * the epilogue computes alpha*acc + beta*C in registers and stores float4s
+//     (scalar stores at ragged edges or when C / ldc is not 16-byte aligned);
+//     with split-K it writes raw partial sums instead.
+//
+// Every mbarrier wait is bounded (see ptx.cuh); a CTA whose wait expires marks
+// the device status word, waits (bounded) for its own TMA copies and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pg {
+namespace {
+
+template <int BN>
+struct FfmaCfg {
+    static constexpr int BM = kBM;
+    static constexpr int BK = kFfmaBK;
+    static constexpr int TGN = BN / 8;                    // thread columns
+    static constexpr int THREADS = 16 * TGN;              // 16 thread rows x TGN
+    static constexpr int CWARPS = THREADS / 32;
+    static constexpr int STAGES = (BN == 128) ? 3 : 4;
+    // While k-block `it` is computed, thread 0 issues k-block it + PD into slot
+    // (it + PD) % STAGES, whose previous contents (k-block it + PD - STAGES) every
+    // warp released STAGES - PD iterations ago; with a spare slot (PD = STAGES-2)
+    // the loader waits only if some warp trails by two whole k-blocks.
+    static constexpr int PD = (STAGES >= 4) ? STAGES - 2 : STAGES - 1;
+    static constexpr int CTAS_PER_SM = (BN == 256) ? 1 : 2;
+    static constexpr int A_BYTES = BM * BK * 4;           // 16 KiB
+    static constexpr int B_BYTES = BN * BK * 4;           // BN rows of 128 B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int BAR_BYTES = 2 * STAGES * 8 + 16;
+    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static_assert(TGN % 8 == 0, "column stride must keep (row % 8) fixed per thread");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128B-swizzle slots need 1 KiB alignment");
+};
+
+__device__ __forceinline__ float comp(const float4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM)
+    ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams p) {
+    using Cfg = FfmaCfg<BN>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + S);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int tile_m, tile_n;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
+    const int64_t m0 = static_cast<int64_t>(tile_m) * Cfg::BM;
+    const int64_t n0 = static_cast<int64_t>(tile_n) * BN;
+    const int slice = blockIdx.y;
+    const int kb0 = slice * p.kb_per_split;
+    const int nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, Cfg::CWARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Thread 0 is also the loader: it issues k-block `it` into slot it % S once
+    // every warp has released that slot's previous contents (k-block it - S).
+    const bool loader = (threadIdx.x == 0) && !(p.debug_flags & 1);
+    int issued = 0;
+    auto issue = [&](int it) -> bool {
+        const int s = it % S;
+        if (!mbar_wait_bounded(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            raise_abort(abort_flag, p.status);
+            return false;
+        }
+        const uint32_t full = full0 + 8 * s;
+        mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+        const int32_t kc = (kb0 + it) * Cfg::BK;
+        const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+        tma_load_2d(slot, &tmA, static_cast<int32_t>(m0), kc, full);
+        tma_load_2d(slot + Cfg::A_BYTES, &tmB, kc, static_cast<int32_t>(n0), full);
+        issued = it + 1;
+        return true;
+    };
+    if (loader) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int it = 0; it < min(Cfg::PD, nkb); ++it)
+            if (!issue(it)) break;
+    }
+
+    // ---------------- consumers ----------------
+    const int wm = warp & 3;
+    const int wn = warp >> 2;
+    const int tm = 4 * wm + (lane >> 3);   // 0..15
+    const int tn = 8 * wn + (lane & 7);    // 0..TGN-1
+    const uint32_t bchunk_xor = static_cast<uint32_t>(tn & 7);
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    bool ok = true;
+    for (int it = 0; it < nkb; ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1;
+        if (loader && issued == it + Cfg::PD && issued < nkb && !*abort_flag) issue(issued);
+        // Every lane waits, then the warp agrees on the outcome so that a lane whose
+        // limit expired a moment earlier cannot leave the others at __syncwarp.
+        const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * s, ph, p.timeout_ns,
+                                                                       abort_flag));
+        if (!landed) {
+            if (lane == 0) raise_abort(abort_flag, p.status);
+            ok = false;
+            break;
+        }
+        const float* As = reinterpret_cast<const float*>(smem + s * Cfg::STAGE_BYTES);
+        const uint8_t* Bs = smem + s * Cfg::STAGE_BYTES + Cfg::A_BYTES + tn * 128;
+#pragma unroll
+        for (int g = 0; g < Cfg::BK / 4; ++g) {
+            float4 b[8];
+            const uint32_t chunk = (static_cast<uint32_t>(g) ^ bchunk_xor) << 4;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                b[jj] = *reinterpret_cast<const float4*>(Bs + jj * (Cfg::TGN * 128) + chunk);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float* arow = As + (4 * g + kk) * Cfg::BM;
+                const float4 a0 = *reinterpret_cast<const float4*>(arow + 4 * tm);
+                const float4 a1 = *reinterpret_cast<const float4*>(arow + 64 + 4 * tm);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) acc[i][jj] = fmaf(a[i], comp(b[jj], kk), acc[i][jj]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+    if (loader) {
+        // The last (up to S) slots issued may still be landing after an abort; do
+        // not let the CTA retire while a copy into its shared memory is in flight.
+        for (int it = max(0, issued - S); it < issued; ++it)
+            mbar_wait_bounded(full0 + 8 * (it % S), (it / S) & 1, p.timeout_ns, nullptr);
+    }
+    if (!ok || *abort_flag) return;
+
+    // ---------------- epilogue ----------------
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+        const int64_t j = n0 + tn + Cfg::TGN * jj;
+        if (j >= p.n) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t i = m0 + 64 * h + 4 * tm;
+            if (i >= p.m) continue;
+            const float v[4] = {acc[4 * h][jj], acc[4 * h + 1][jj], acc[4 * h + 2][jj], acc[4 * h + 3][jj]};
+            if (p.split > 1) {
+                float* dst = p.P + slice * p.p_stride + j * p.ldp + i;
+                if (i + 3 < p.m) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+                    for (int e = 0; e < 4; ++e)
+                        if (i + e < p.m) dst[e] = v[e];
+                }
+            } else {
+                float* dst = p.C + j * p.ldc + i;
+                if (p.c_vec && i + 3 < p.m) {
+                    float4 o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                    if (beta != 0.0f) {
+                        const float4 c = *reinterpret_cast<const float4*>(dst);
+                        o.x = fmaf(beta, c.x, o.x);
+                        o.y = fmaf(beta, c.y, o.y);
+                        o.z = fmaf(beta, c.z, o.z);
+                        o.w = fmaf(beta, c.w, o.w);
+                    }
+                    *reinterpret_cast<float4*>(dst) = o;
+                } else {
+                    for (int e = 0; e < 4; ++e) {
+                        if (i + e >= p.m) break;
+                        float o = alpha * v[e];
+                        if (beta != 0.0f) o = fmaf(beta, dst[e], o);
+                        dst[e] = o;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int BN>
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, dim3 grid,
+                        cudaStream_t stream) {
+    using Cfg = FfmaCfg<BN>;
+    auto kern = ffma_gemm_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::SMEM));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int ffma_threads(int bn) {
+    return bn == 64 ? FfmaCfg<64>::THREADS : bn == 128 ? FfmaCfg<128>::THREADS : FfmaCfg<256>::THREADS;
+}
+int ffma_stages(int bn) {
+    return bn == 64 ? FfmaCfg<64>::STAGES : bn == 128 ? FfmaCfg<128>::STAGES : FfmaCfg<256>::STAGES;
+}
+int ffma_ctas_per_sm(int bn) {
+    return bn == 64 ? FfmaCfg<64>::CTAS_PER_SM
+                    : bn == 128 ? FfmaCfg<128>::CTAS_PER_SM : FfmaCfg<256>::CTAS_PER_SM;
+}
+size_t ffma_smem_bytes(int bn) {
+    return bn == 64 ? FfmaCfg<64>::SMEM : bn == 128 ? FfmaCfg<128>::SMEM : FfmaCfg<256>::SMEM;
+}
+
+cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn,
+                        dim3 grid, cudaStream_t stream) {
+    switch (bn) {
+        case 64: return launch_impl<64>(tmA, tmB, p, grid, stream);
+        case 128: return launch_impl<128>(tmA, tmB, p, grid, stream);
+        case 256: return launch_impl<256>(tmA, tmB, p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pg

@@ -1,0 +1,72 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (header only; the driver is reached at run time)
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pg {
+
+// Tile geometry common to every GEMM kernel: BM rows of C per CTA.
+constexpr int kBM = 128;
+// FFMA kernel: K block staged per ring slot.
+constexpr int kFfmaBK = 32;
+
+// Parameters every GEMM kernel receives (by value, in the kernel's param space).
+struct GemmParams {
+    int64_t m, n, k;
+    float alpha, beta;
+    float* C;            // final output (split == 1)
+    int64_t ldc;
+    float* P;            // partial sums [split][n][ldp] (split > 1)
+    int64_t ldp;         // multiple of 4
+    int64_t p_stride;    // elements between two slices of P (= ldp * n)
+    int32_t tiles_m, tiles_n;
+    int32_t kb_total;        // K blocks in total
+    int32_t kb_per_split;    // K blocks per slice
+    int32_t split;           // number of slices
+    int32_t group_m;         // rasterisation: tile rows per group
+    int32_t c_vec;           // C 16-byte aligned and ldc % 4 == 0
+    int32_t debug_flags;
+    uint64_t timeout_ns;     // limit of every bounded wait
+    int* status;             // per-device status word
+};
+
+// Device status values written by kernels (match SGEMM_ERR_* of the ABI).
+constexpr int kStatusTimeout = 4;
+
+// ---- launchers (each lives beside its kernel) -------------------------------
+
+// FFMA kernel: tile 128 x bn, bn in {64, 128, 256}.
+int ffma_threads(int bn);
+int ffma_stages(int bn);
+int ffma_ctas_per_sm(int bn);
+size_t ffma_smem_bytes(int bn);
+cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                        int bn, dim3 grid, cudaStream_t stream);
+
+// tcgen05 kernel: tile 128 x bn, bn in {64, 128, 256}; split3 selects 3xTF32.
+int tc_bk(bool split3);
+int tc_stages(int bn, bool split3);
+int tc_threads();
+size_t tc_smem_bytes(int bn, bool split3);
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
+                      const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3,
+                      dim3 grid, cudaStream_t stream);
+
+// Operand preparation: dst(r, c) = src(r, c) (or src(c, r) when transposed) for
+// r < rows, c < cols, dst with leading dimension ldd.  With dst_small != null
+// the value is split into a TF32 "big" part (dst) and the exact remainder
+// (dst_small).
+cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t rows,
+                        int64_t cols, float* dst, float* dst_small, int64_t ldd,
+                        int num_sms, cudaStream_t stream);
+
+// C = alpha * sum_s P[s] + beta * C, slices summed in increasing s.
+cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// C = beta * C (beta == 0 writes zeros without reading C).
+cudaError_t launch_scale(float* C, int64_t ldc, int64_t m, int64_t n, float beta, int num_sms,
+                         cudaStream_t stream);
+
+}  // namespace pg

@@ -1,0 +1,518 @@
+// C ABI of the library (declared in include/precision_gemm.h): argument checks,
+// planning (kernel, tile, split-K, operand preparation), the per-(device,
+// stream) workspace, TMA tensor-map encoding and the launch sequence.
+//
+// The host-side flow follows the lecture's matmatgpu1 ("HPC - Lecture 13 -
+// MatMat GPU"): operands with leading dimensions are brought into the layout the
+// kernel wants, the kernel runs, and C is written back -- except that here the
+// operands already live on the device, the "packing" is a device pre-pass that
+// runs only when TMA cannot read an operand in place, and nothing is copied
+// through the host (sgemm_host is the variant that starts from host arrays).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/precision_gemm.h"
+#include "internal.h"
+
+#define PG_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace pg {
+
+// Per-device status word written by kernels whose bounded wait expired.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr const char* kVersion = "precision_gemm_gb300 0.1.0 (sm_103a; FFMA, TF32, 3xTF32)";
+
+thread_local char t_err[512] = "no error";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+    return fail(SGEMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<int> g_force_bn{0};
+std::atomic<int> g_force_split{0};
+std::atomic<int> g_debug{0};
+std::atomic<uint64_t> g_launches{0};
+
+bool is_notrans(char t) { return t == 'N' || t == 'n'; }
+bool valid_trans(char t) { return t == 'N' || t == 'n' || t == 'T' || t == 't' || t == 'C' || t == 'c'; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;  // TMA coordinates (tile + box) are 32-bit
+constexpr int64_t kMaxLd = (int64_t(1) << 37);        // TMA strides are < 2^40 bytes
+
+// Checks in the order of the signature; returns 0 or -i.
+int validate(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+             int64_t lda, const void* B, int64_t ldb, float beta, const void* C, int64_t ldc, int mode) {
+    if (!valid_trans(transa)) return fail(-1, "argument 1 (transa): '%c' is not N, T or C", transa);
+    if (!valid_trans(transb)) return fail(-2, "argument 2 (transb): '%c' is not N, T or C", transb);
+    if (m < 0 || m > kMaxDim) return fail(-3, "argument 3 (m): %lld out of [0, 2^31-1024]", (long long)m);
+    if (n < 0 || n > kMaxDim) return fail(-4, "argument 4 (n): %lld out of [0, 2^31-1024]", (long long)n);
+    if (k < 0 || k > kMaxDim) return fail(-5, "argument 5 (k): %lld out of [0, 2^31-1024]", (long long)k);
+    const bool reads_ab = m > 0 && n > 0 && k > 0 && alpha != 0.0f;
+    if (reads_ab && A == nullptr) return fail(-7, "argument 7 (A): null pointer");
+    const int64_t rows_a = is_notrans(transa) ? m : k;
+    if (lda < std::max<int64_t>(1, rows_a) || lda > kMaxLd)
+        return fail(-8, "argument 8 (lda): %lld < max(1, %lld) or too large", (long long)lda, (long long)rows_a);
+    if (reads_ab && B == nullptr) return fail(-9, "argument 9 (B): null pointer");
+    const int64_t rows_b = is_notrans(transb) ? k : n;
+    if (ldb < std::max<int64_t>(1, rows_b) || ldb > kMaxLd)
+        return fail(-10, "argument 10 (ldb): %lld < max(1, %lld) or too large", (long long)ldb, (long long)rows_b);
+    const bool touches_c = m > 0 && n > 0 && (reads_ab || beta != 1.0f);
+    if (touches_c && C == nullptr) return fail(-12, "argument 12 (C): null pointer");
+    if (ldc < std::max<int64_t>(1, m) || ldc > kMaxLd)
+        return fail(-13, "argument 13 (ldc): %lld < max(1, %lld) or too large", (long long)ldc, (long long)m);
+    if (mode != SGEMM_FFMA && mode != SGEMM_TF32 && mode != SGEMM_3XTF32)
+        return fail(-14, "argument 14 (mode): %d is not SGEMM_FFMA, SGEMM_TF32 or SGEMM_3XTF32", mode);
+    (void)beta;
+    return 0;
+}
+
+size_t region(int64_t elems) { return static_cast<size_t>(round_up(elems * 4, 256)); }
+
+// The planner.  Pure host arithmetic: no device is touched.
+void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+               int64_t lda, const void* B, int64_t ldb, float beta, int mode, int num_sms, sgemm_plan_t* pl) {
+    std::memset(pl, 0, sizeof *pl);
+    pl->mode = mode;
+    pl->split_k = 1;
+    pl->bm = kBM;
+    if (m == 0 || n == 0) {
+        pl->kernel = SGEMM_KERNEL_NONE;
+        return;
+    }
+    if (k == 0 || alpha == 0.0f) {
+        pl->kernel = (beta == 1.0f) ? SGEMM_KERNEL_NONE : SGEMM_KERNEL_SCALE;
+        pl->launches = (pl->kernel == SGEMM_KERNEL_SCALE) ? 1 : 0;
+        return;
+    }
+    const bool tc = mode != SGEMM_FFMA;
+    const bool split3 = mode == SGEMM_3XTF32;
+
+    // Operand preparation: TMA needs a 16-byte aligned base and a leading
+    // dimension that is a multiple of 16 bytes; the kernels read A M-major and
+    // B K-major, i.e. both not transposed.
+    const bool a_inplace = is_notrans(transa) && aligned16(A) && (lda % 4 == 0);
+    const bool b_inplace = is_notrans(transb) && aligned16(B) && (ldb % 4 == 0);
+    if (split3) {
+        pl->prep_a = SGEMM_PREP_SPLIT;
+        pl->prep_b = SGEMM_PREP_SPLIT;
+    } else {
+        pl->prep_a = a_inplace ? SGEMM_PREP_NONE : (is_notrans(transa) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
+        pl->prep_b = b_inplace ? SGEMM_PREP_NONE : (is_notrans(transb) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
+    }
+    pl->ld_a = pl->prep_a == SGEMM_PREP_NONE ? lda : round_up(m, 4);
+    pl->ld_b = pl->prep_b == SGEMM_PREP_NONE ? ldb : round_up(k, 4);
+
+    // Tile width: the narrowest of 64/128/256 that covers n, else 256.
+    int bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
+    const int fbn = g_force_bn.load();
+    if (fbn) bn = fbn;
+    pl->bn = bn;
+    pl->kernel = tc ? SGEMM_KERNEL_TC : SGEMM_KERNEL_FFMA;
+    pl->bk = tc ? tc_bk(split3) : kFfmaBK;
+    pl->stages = tc ? tc_stages(bn, split3) : ffma_stages(bn);
+    pl->threads = tc ? tc_threads() : ffma_threads(bn);
+    pl->ctas_per_sm = tc ? 1 : ffma_ctas_per_sm(bn);
+    pl->smem_bytes = tc ? tc_smem_bytes(bn, split3) : ffma_smem_bytes(bn);
+    pl->tiles_m = static_cast<int>(cdiv(m, kBM));
+    pl->tiles_n = static_cast<int>(cdiv(n, bn));
+    pl->k_blocks = static_cast<int>(cdiv(k, pl->bk));
+
+    // Split-K when the output tiles cannot fill one wave of the machine: give
+    // each tile floor(capacity / tiles) K slices of at least 4 K blocks each.
+    const int64_t tiles = static_cast<int64_t>(pl->tiles_m) * pl->tiles_n;
+    const int64_t capacity = static_cast<int64_t>(std::max(num_sms, 1)) * pl->ctas_per_sm;
+    int64_t split = 1;
+    const int fs = g_force_split.load();
+    if (fs > 0) {
+        split = fs;
+    } else if (tiles < capacity) {
+        split = std::min<int64_t>(capacity / tiles, pl->k_blocks / 4);
+    }
+    split = std::max<int64_t>(1, std::min<int64_t>({split, static_cast<int64_t>(pl->k_blocks), 65535}));
+    const int64_t per = cdiv(pl->k_blocks, split);
+    split = cdiv(pl->k_blocks, per);  // no empty slice
+    pl->split_k = static_cast<int>(split);
+    pl->k_blocks_per_split = static_cast<int>(per);
+
+    size_t ws = 0;
+    const int parts = split3 ? 2 : 1;
+    if (pl->prep_a != SGEMM_PREP_NONE) ws += parts * region(pl->ld_a * k);
+    if (pl->prep_b != SGEMM_PREP_NONE) ws += parts * region(pl->ld_b * n);
+    if (split > 1) ws += region(split * round_up(m, 4) * n);
+    pl->workspace_bytes = ws;
+    pl->launches = (pl->prep_a != SGEMM_PREP_NONE) + (pl->prep_b != SGEMM_PREP_NONE) + 1 + (split > 1);
+}
+
+// ---- devices ------------------------------------------------------------------------
+
+struct DeviceState {
+    bool init = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+    int* status = nullptr;
+};
+std::mutex g_dev_mu;
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int* dev_out, DeviceState** ds_out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return fail(SGEMM_ERR_NO_DEVICE, "no usable CUDA device: %s", cudaGetErrorString(e));
+    }
+    if (dev >= kMaxDevices) return fail(SGEMM_ERR_NO_DEVICE, "device ordinal %d unsupported", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return fail_cuda(e, "cudaDeviceGetAttribute");
+        if (d.major == 10 && d.minor == 3) {
+            if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_device_status)) != cudaSuccess)
+                return fail_cuda(e, "cudaGetSymbolAddress(status word)");
+        }
+        d.init = true;
+    }
+    if (!(d.major == 10 && d.minor == 3))
+        return fail(SGEMM_ERR_ARCH, "device %d is compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                    dev, d.major, d.minor);
+    *dev_out = dev;
+    *ds_out = &d;
+    return 0;
+}
+
+// ---- workspace: one growing buffer per (device, stream, purpose) ---------------------
+
+struct Buf {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<std::pair<int, uintptr_t>, int>, Buf> g_bufs;
+
+int get_buffer(int dev, cudaStream_t st, int purpose, size_t need, void** out) {
+    *out = nullptr;
+    if (need == 0) return 0;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Buf& b = g_bufs[{{dev, reinterpret_cast<uintptr_t>(st)}, purpose}];
+    if (b.bytes >= need) {
+        *out = b.ptr;
+        return 0;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(SGEMM_ERR_CAPTURE,
+                    "workspace must grow to %zu bytes during stream capture; make one call of this size "
+                    "before capturing", need);
+    if (b.ptr) {
+        if ((e = cudaFreeAsync(b.ptr, st)) != cudaSuccess) return fail_cuda(e, "cudaFreeAsync(workspace)");
+        b.ptr = nullptr;
+        b.bytes = 0;
+    }
+    const size_t bytes = static_cast<size_t>(round_up(static_cast<int64_t>(need), int64_t(2) << 20));
+    if ((e = cudaMallocAsync(&b.ptr, bytes, st)) != cudaSuccess) {
+        cudaGetLastError();
+        b.ptr = nullptr;
+        return fail(SGEMM_ERR_ALLOC, "cudaMallocAsync(%zu bytes) for the workspace: %s", bytes, cudaGetErrorString(e));
+    }
+    b.bytes = bytes;
+    *out = b.ptr;
+    return 0;
+}
+
+constexpr int kPurposeWorkspace = 0;
+constexpr int kPurposeStaging = 1;
+
+// ---- TMA tensor maps ------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D fp32 column-major matrix rows x cols with leading dimension ld (elements),
+// box {box_rows, box_cols}; out-of-range elements of a box read as zero.
+int encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
+              uint32_t box_cols, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    const cuuint32_t box[2] = {box_rows, box_cols};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld matrix, ld %lld",
+                    static_cast<int>(r), (long long)rows, (long long)cols, (long long)ld);
+    return 0;
+}
+
+// ---- the call ---------------------------------------------------------------------------
+
+int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
+        const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode, cudaStream_t st) {
+    int dev;
+    DeviceState* ds;
+    int rc = current_device(&dev, &ds);
+    if (rc) return rc;
+    sgemm_plan_t pl;
+    make_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, mode, ds->sms, &pl);
+    cudaError_t e;
+    if (pl.kernel == SGEMM_KERNEL_NONE) return 0;
+    if (pl.kernel == SGEMM_KERNEL_SCALE) {
+        if ((e = launch_scale(C, ldc, m, n, beta, ds->sms, st)) != cudaSuccess) return fail_cuda(e, "scale kernel");
+        g_launches += 1;
+        return 0;
+    }
+    void* ws = nullptr;
+    if ((rc = get_buffer(dev, st, kPurposeWorkspace, pl.workspace_bytes, &ws))) return rc;
+    const bool split3 = mode == SGEMM_3XTF32;
+    const int parts = split3 ? 2 : 1;
+    char* cursor = static_cast<char*>(ws);
+
+    const float* a_big = A;
+    const float* a_small = nullptr;
+    if (pl.prep_a != SGEMM_PREP_NONE) {
+        float* d = reinterpret_cast<float*>(cursor);
+        cursor += region(pl.ld_a * k);
+        float* ds2 = nullptr;
+        if (parts == 2) {
+            ds2 = reinterpret_cast<float*>(cursor);
+            cursor += region(pl.ld_a * k);
+        }
+        if ((e = launch_prep(A, lda, !is_notrans(transa), m, k, d, ds2, pl.ld_a, ds->sms, st)) != cudaSuccess)
+            return fail_cuda(e, "operand preparation (A)");
+        a_big = d;
+        a_small = ds2;
+    }
+    const float* b_big = B;
+    const float* b_small = nullptr;
+    if (pl.prep_b != SGEMM_PREP_NONE) {
+        float* d = reinterpret_cast<float*>(cursor);
+        cursor += region(pl.ld_b * n);
+        float* ds2 = nullptr;
+        if (parts == 2) {
+            ds2 = reinterpret_cast<float*>(cursor);
+            cursor += region(pl.ld_b * n);
+        }
+        if ((e = launch_prep(B, ldb, !is_notrans(transb), k, n, d, ds2, pl.ld_b, ds->sms, st)) != cudaSuccess)
+            return fail_cuda(e, "operand preparation (B)");
+        b_big = d;
+        b_small = ds2;
+    }
+
+    GemmParams gp{};
+    gp.m = m;
+    gp.n = n;
+    gp.k = k;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.C = C;
+    gp.ldc = ldc;
+    gp.split = pl.split_k;
+    if (pl.split_k > 1) {
+        gp.P = reinterpret_cast<float*>(cursor);
+        gp.ldp = round_up(m, 4);
+        gp.p_stride = gp.ldp * n;
+    }
+    gp.tiles_m = pl.tiles_m;
+    gp.tiles_n = pl.tiles_n;
+    gp.kb_total = pl.k_blocks;
+    gp.kb_per_split = pl.k_blocks_per_split;
+    gp.group_m = 16;
+    gp.c_vec = aligned16(C) && (ldc % 4 == 0);
+    gp.debug_flags = g_debug.load();
+    gp.timeout_ns = g_timeout_ns.load();
+    gp.status = ds->status;
+
+    const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
+    CUtensorMap tmA, tmB, tmAs, tmBs;
+    if (pl.kernel == SGEMM_KERNEL_FFMA) {
+        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
+        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+        if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");
+    } else {
+        const CUtensorMapSwizzle bsw = pl.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))) return rc;
+        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, pl.bk, pl.bn, bsw))) return rc;
+        tmAs = tmA;
+        tmBs = tmB;
+        if (split3) {
+            if ((rc = encode_2d(&tmAs, a_small, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)))
+                return rc;
+            if ((rc = encode_2d(&tmBs, b_small, k, n, pl.ld_b, pl.bk, pl.bn, bsw))) return rc;
+        }
+        if ((e = launch_tc(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
+            return fail_cuda(e, "tcgen05 GEMM kernel");
+    }
+    if (pl.split_k > 1) {
+        if ((e = launch_splitk_reduce(gp, ds->sms, st)) != cudaSuccess) return fail_cuda(e, "split-K reduction");
+    }
+    g_launches += pl.launches;
+    return 0;
+}
+
+}  // namespace
+}  // namespace pg
+
+using namespace pg;
+
+PG_EXPORT int sgemm(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
+                    int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
+                    void* stream) {
+    int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
+    if (rc) return rc;
+    if (m == 0 || n == 0 || ((k == 0 || alpha == 0.0f) && beta == 1.0f)) return 0;  // C unchanged
+    return run(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode,
+               static_cast<cudaStream_t>(stream));
+}
+
+PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
+                         void* stream) {
+    int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
+    if (rc) return rc;
+    if (m == 0 || n == 0) return 0;
+    int dev;
+    DeviceState* ds;
+    if ((rc = current_device(&dev, &ds))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool reads_ab = k > 0 && alpha != 0.0f;
+    const int64_t ra = is_notrans(transa) ? m : k, ca = is_notrans(transa) ? k : m;
+    const int64_t rb = is_notrans(transb) ? k : n, cb = is_notrans(transb) ? n : k;
+    const int64_t lda_d = round_up(ra, 4), ldb_d = round_up(rb, 4), ldc_d = round_up(m, 4);
+    const size_t a_bytes = reads_ab ? region(lda_d * ca) : 0;
+    const size_t b_bytes = reads_ab ? region(ldb_d * cb) : 0;
+    const size_t c_bytes = region(ldc_d * n);
+    void* stage = nullptr;
+    if ((rc = get_buffer(dev, st, kPurposeStaging, a_bytes + b_bytes + c_bytes, &stage))) return rc;
+    float* dA = reinterpret_cast<float*>(static_cast<char*>(stage));
+    float* dB = reinterpret_cast<float*>(static_cast<char*>(stage) + a_bytes);
+    float* dC = reinterpret_cast<float*>(static_cast<char*>(stage) + a_bytes + b_bytes);
+    cudaError_t e;
+    if (reads_ab) {
+        if ((e = cudaMemcpy2DAsync(dA, lda_d * 4, A, lda * 4, ra * 4, ca, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return fail_cuda(e, "copy of A to the device");
+        if ((e = cudaMemcpy2DAsync(dB, ldb_d * 4, B, ldb * 4, rb * 4, cb, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return fail_cuda(e, "copy of B to the device");
+    }
+    if (beta != 0.0f) {
+        if ((e = cudaMemcpy2DAsync(dC, ldc_d * 4, C, ldc * 4, m * 4, n, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return fail_cuda(e, "copy of C to the device");
+    }
+    rc = run(transa, transb, m, n, k, alpha, reads_ab ? dA : nullptr, reads_ab ? lda_d : 1, reads_ab ? dB : nullptr,
+             reads_ab ? ldb_d : 1, beta, dC, ldc_d, mode, st);
+    if (rc) return rc;
+    if ((e = cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_d * 4, m * 4, n, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return fail_cuda(e, "copy of C to the host");
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    return 0;
+}
+
+PG_EXPORT int sgemm_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                         int64_t lda, const void* B, int64_t ldb, float beta, const void* C, int64_t ldc, int mode,
+                         int num_sms, sgemm_plan_t* plan) {
+    int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
+    if (rc) return rc;
+    if (num_sms <= 0) return fail(-15, "argument 15 (num_sms): %d must be positive", num_sms);
+    if (plan == nullptr) return fail(-16, "argument 16 (plan): null pointer");
+    make_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, mode, num_sms, plan);
+    return 0;
+}
+
+PG_EXPORT int sgemm_device_status(void* stream, int clear) {
+    int dev;
+    DeviceState* ds;
+    int rc = current_device(&dev, &ds);
+    if (rc) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    int v = 0;
+    if ((e = cudaMemcpy(&v, ds->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail_cuda(e, "reading the status word");
+    if (clear && (e = cudaMemset(ds->status, 0, sizeof v)) != cudaSuccess) return fail_cuda(e, "clearing the status word");
+    if (v != 0) return fail(v, "a kernel on device %d recorded status %d (bounded wait expired)", dev, v);
+    return 0;
+}
+
+PG_EXPORT uint64_t sgemm_set_wait_timeout(uint64_t ns) { return g_timeout_ns.exchange(ns); }
+
+PG_EXPORT int sgemm_force_plan(int bn, int split_k) {
+    if (!(bn == 0 || bn == 64 || bn == 128 || bn == 256)) return fail(-1, "bn %d is not 0, 64, 128 or 256", bn);
+    if (split_k < 0) return fail(-2, "split_k %d is negative", split_k);
+    g_force_bn = bn;
+    g_force_split = split_k;
+    return 0;
+}
+
+PG_EXPORT int sgemm_debug_flags(int flags) { return g_debug.exchange(flags); }
+
+PG_EXPORT uint64_t sgemm_launch_count(void) { return g_launches.load(); }
+
+PG_EXPORT int sgemm_workspace_release(void) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int prev = -1;
+    cudaGetDevice(&prev);
+    int rc = 0;
+    for (auto& kv : g_bufs) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first.first);
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaFree(kv.second.ptr);
+        if (e != cudaSuccess && !rc) rc = fail_cuda(e, "releasing the workspace");
+        kv.second = Buf{};
+    }
+    g_bufs.clear();
+    if (prev >= 0) cudaSetDevice(prev);
+    return rc;
+}
+
+PG_EXPORT const char* sgemm_last_error_string(void) { return t_err; }
+
+PG_EXPORT const char* sgemm_version(void) { return kVersion; }

@@ -1,0 +1,302 @@
+// Tensor-core GEMM (tcgen05, sm_103a): TF32 and 3xTF32 modes.
+//
+// One CTA computes a 128 x BN tile of C with the fifth-generation tensor cores:
+// operands are staged in shared memory by TMA, one elected thread issues
+// tcgen05.mma (M = 128, N = BN, K = 8 per instruction) into an FP32 accumulator
+// held in tensor memory (TMEM), and four epilogue warps read the accumulator
+// back with tcgen05.ld and apply alpha/beta.  The pages' tensor-core prior art
+// ("cuda-kernel-opt": asynchronous loads, consumer warps decoupled from each
+// other, accumulators tuned per warp) is superseded here: a single issuing
+// thread replaces per-warp MMA fragments, so the pages' per-warp "shift"
+// barriers have nothing left to order.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA loader (one thread): A as four 32-row boxes, B as one box
+//   warp 1      allocates TMEM; one thread issues the MMAs; frees TMEM at exit
+//   warps 2-5   epilogue; warp w may access TMEM lanes 32*(w%4) .. +31
+//
+// Shared-memory operand layouts (canonical tcgen05 layouts, 1 KiB aligned):
+//   A (column-major, M-major): per 32-row group of M a box of BK rows of k,
+//     each row 32 floats = 128 B, in the 128-byte swizzle with 32-byte atoms
+//     (TMA SWIZZLE_128B_ATOM_32B; descriptor layout 1) -- the form tcgen05 takes
+//     for an M-major TF32 operand (measured: the plain 128-byte swizzle reads as
+//     zeros for M-major TF32).  Leading byte offset (between 32-row groups of M)
+//     = 128*BK, stride byte offset (between 4-row atoms of k) = 512.  The k-step
+//     kk (8 values, two atoms) starts at +1024*kk.
+//   B (column-major, K-major): BN rows of BK floats; BK = 32 -> 128-byte rows
+//     with the 128-byte swizzle (8-row groups of 1024 B); BK = 16 -> 64-byte
+//     rows with the 64-byte swizzle (groups of 512 B).  The k-step kk starts at
+//     +32*kk bytes inside the swizzle atom.
+//
+// 3xTF32 (SPLIT3): each operand arrives as a "big" TF32 part and the exact
+// remainder ("small"), prepared by the split pre-pass; per k-step the thread
+// issues small*big, big*small, big*big into the same accumulator (the
+// small*small term is below FP32 resolution and dropped).  Four operand tiles
+// per slot halve BK to 16 so four slots still fit.
+//
+// Every wait is bounded; on expiry the CTA records the status, lets its
+// in-flight TMA copies and MMAs finish (bounded), frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pg {
+namespace {
+
+template <int BN, bool SPLIT3>
+struct TcCfg {
+    static constexpr int BM = kBM;
+    static constexpr int BK = SPLIT3 ? 16 : 32;
+    static constexpr int OPS = SPLIT3 ? 2 : 1;   // parts per operand
+    static constexpr int A_BYTES = BM * BK * 4;  // one part of A
+    static constexpr int B_BYTES = BN * BK * 4;  // one part of B
+    static constexpr int A_BOX_BYTES = 32 * BK * 4;
+    static constexpr int STAGE_BYTES = OPS * (A_BYTES + B_BYTES);
+    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int THREADS = 192;
+    static constexpr int BAR_BYTES = (2 * STAGES + 1) * 8 + 16;
+    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_tf32(BM, BN, /*a_mn_major=*/true, /*b_mn_major=*/false);
+    static constexpr uint32_t A_LBO = 128 * BK;
+    static constexpr uint32_t A_SBO = 512;
+    static constexpr uint32_t B_SBO = (BK == 32) ? 1024 : 512;
+    static constexpr uint32_t B_LAYOUT = (BK == 32) ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t TMEM_COLS = BN;  // power of two >= 32
+    static_assert(STAGES >= 2, "ring too shallow");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+};
+
+template <int BN, bool SPLIT3>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
+                   const GemmParams p) {
+    using Cfg = TcCfg<BN, SPLIT3>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + S);
+    const uint32_t accum_bar = smem_u32(bars + 2 * S);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int tile_m, tile_n;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
+    const int64_t m0 = static_cast<int64_t>(tile_m) * Cfg::BM;
+    const int64_t n0 = static_cast<int64_t>(tile_n) * BN;
+    const int slice = blockIdx.y;
+    const int kb0 = slice * p.kb_per_split;
+    const int nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(accum_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- TMA loader ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+            if (SPLIT3) {
+                prefetch_tmap(&tmAs);
+                prefetch_tmap(&tmBs);
+            }
+            int issued = 0;
+            if (!(p.debug_flags & 1)) {
+                for (int it = 0; it < nkb; ++it) {
+                    const int s = it % S;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                        raise_abort(abort_flag, p.status);
+                        break;
+                    }
+                    const uint32_t full = full0 + 8 * s;
+                    mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+                    const int32_t kc = (kb0 + it) * Cfg::BK;
+                    const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_2d(slot + g * Cfg::A_BOX_BYTES, &tmA, static_cast<int32_t>(m0 + 32 * g), kc,
+                                    full);
+                    uint32_t b_slot = slot + Cfg::A_BYTES;
+                    if (SPLIT3) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            tma_load_2d(slot + Cfg::A_BYTES + g * Cfg::A_BOX_BYTES, &tmAs,
+                                        static_cast<int32_t>(m0 + 32 * g), kc, full);
+                        b_slot = slot + 2 * Cfg::A_BYTES;
+                        tma_load_2d(b_slot + Cfg::B_BYTES, &tmBs, kc, static_cast<int32_t>(n0), full);
+                    }
+                    tma_load_2d(b_slot, &tmB, kc, static_cast<int32_t>(n0), full);
+                    issued = it + 1;
+                }
+            }
+            // Let every copy this CTA issued land before it may retire.
+            for (int it = max(0, issued - S); it < issued; ++it)
+                mbar_wait_bounded(full0 + 8 * (it % S), (it / S) & 1, p.timeout_ns, nullptr);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t accumulate = 0;
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % S;
+                if (!mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
+                    raise_abort(abort_flag, p.status);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+                const uint32_t a_big = slot;
+                const uint32_t a_small = slot + Cfg::A_BYTES;
+                const uint32_t b_big = slot + Cfg::OPS * Cfg::A_BYTES;
+                const uint32_t b_small = b_big + Cfg::B_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
+                    const uint64_t ad = smem_desc(a_big + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
+                    const uint64_t bd = smem_desc(b_big + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
+                    if (SPLIT3) {
+                        const uint64_t asd =
+                            smem_desc(a_small + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
+                        const uint64_t bsd = smem_desc(b_small + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
+                        mma_tf32(tmem, asd, bd, Cfg::IDESC, accumulate);
+                        accumulate = 1;
+                        mma_tf32(tmem, ad, bsd, Cfg::IDESC, 1);
+                        mma_tf32(tmem, ad, bd, Cfg::IDESC, 1);
+                    } else {
+                        mma_tf32(tmem, ad, bd, Cfg::IDESC, accumulate);
+                        accumulate = 1;
+                    }
+                }
+                mma_commit(empty0 + 8 * s);  // slot reusable once these MMAs have read it
+            }
+            mma_commit(accum_bar);  // accumulator complete (also after an abort)
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;
+        const bool ready =
+            __all_sync(0xffffffffu, mbar_wait_bounded(accum_bar, 0, p.timeout_ns, abort_flag));
+        if (!ready) {
+            if (lane == 0) raise_abort(abort_flag, p.status);
+        } else if (!*abort_flag) {
+            tc_fence_after_sync();
+            const int64_t i = m0 + 32 * q + lane;
+            const bool row_ok = i < p.m;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+            const float alpha = p.alpha, beta = p.beta;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int64_t jb = n0 + 32 * c;
+                if (jb >= p.n) break;  // uniform across the warp
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(lane_base + 32 * c, v);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
+                if (p.split > 1) {
+                    float* dst = p.P + slice * p.p_stride + jb * p.ldp + i;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (t < jn) dst[t * p.ldp] = __uint_as_float(v[t]);
+                } else {
+                    float* dst = p.C + jb * p.ldc + i;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        if (t < jn) {
+                            float o = alpha * __uint_as_float(v[t]);
+                            if (beta != 0.0f) o = fmaf(beta, dst[t * p.ldc], o);
+                            dst[t * p.ldc] = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        if (*abort_flag) {
+            // MMAs issued before an abort must finish before TMEM is released.
+            if (lane == 0) mbar_wait_bounded(accum_bar, 0, p.timeout_ns, nullptr);
+            __syncwarp();
+        }
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+template <int BN, bool SPLIT3>
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
+                        const CUtensorMap& tmBs, const GemmParams& p, dim3 grid, cudaStream_t stream) {
+    using Cfg = TcCfg<BN, SPLIT3>;
+    auto kern = tc_gemm_kernel<BN, SPLIT3>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::SMEM));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmAs, tmB, tmBs, p);
+    return cudaGetLastError();
+}
+
+template <bool SPLIT3>
+cudaError_t launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b,
+                      const CUtensorMap& bs, const GemmParams& p, dim3 grid, cudaStream_t st) {
+    switch (bn) {
+        case 64: return launch_impl<64, SPLIT3>(a, as, b, bs, p, grid, st);
+        case 128: return launch_impl<128, SPLIT3>(a, as, b, bs, p, grid, st);
+        case 256: return launch_impl<256, SPLIT3>(a, as, b, bs, p, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <bool SPLIT3>
+constexpr int stages_of(int bn) {
+    return bn == 64 ? TcCfg<64, SPLIT3>::STAGES
+                    : bn == 128 ? TcCfg<128, SPLIT3>::STAGES : TcCfg<256, SPLIT3>::STAGES;
+}
+
+template <bool SPLIT3>
+constexpr size_t smem_of(int bn) {
+    return bn == 64 ? TcCfg<64, SPLIT3>::SMEM : bn == 128 ? TcCfg<128, SPLIT3>::SMEM : TcCfg<256, SPLIT3>::SMEM;
+}
+
+}  // namespace
+
+int tc_bk(bool split3) { return split3 ? TcCfg<256, true>::BK : TcCfg<256, false>::BK; }
+int tc_stages(int bn, bool split3) { return split3 ? stages_of<true>(bn) : stages_of<false>(bn); }
+int tc_threads() { return 192; }
+size_t tc_smem_bytes(int bn, bool split3) { return split3 ? smem_of<true>(bn) : smem_of<false>(bn); }
+
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
+                      const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3, dim3 grid,
+                      cudaStream_t stream) {
+    return split3 ? launch_bn<true>(bn, tmA, tmAs, tmB, tmBs, p, grid, stream)
+                  : launch_bn<false>(bn, tmA, tmAs, tmB, tmBs, p, grid, stream);
+}
+
+}  // namespace pg

@@ -1,0 +1,174 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function the header declares, rejects invalid arguments with -i before
+touching a device, and the planner makes the documented choices."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import precision_gemm_gb300 as pg
+from precision_gemm_gb300 import build as pgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "precision_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pgbuild.build()
+    return pg.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sgemm\w*)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(pg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", pg.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted(line.split()[-1] for line in out.splitlines() if " T " in line)
+    assert exported == _declared_functions()
+
+
+def test_version(lib):
+    assert "sm_103a" in pg.version()
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "precision_gemm.h"\nint main(void){ sgemm_plan_t p; (void)p; '
+                   'return sgemm_version() == 0; }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c",
+                        str(src), "-o", str(tmp_path / "use.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+# Arguments: (transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode)
+GOOD = ("N", "N", 64, 48, 32, 1.0, 4096, 64, 8192, 32, 0.0, 16384, 64, 0)
+
+
+def _call(lib, args):
+    ta, tb, m, n, k, al, A, lda, B, ldb, be, C, ldc, mode = args
+    return lib.sgemm(ta.encode(), tb.encode(), m, n, k, al, A, lda, B, ldb, be, C, ldc, mode, None)
+
+
+def _with(**kw):
+    names = ("transa", "transb", "m", "n", "k", "alpha", "A", "lda", "B", "ldb", "beta", "C", "ldc", "mode")
+    vals = dict(zip(names, GOOD))
+    vals.update(kw)
+    return tuple(vals[n] for n in names)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(transa="X"), -1), (dict(transb="q"), -2), (dict(m=-1), -3), (dict(n=-5), -4), (dict(k=-2), -5),
+    (dict(m=2 ** 31), -3), (dict(A=0), -7), (dict(lda=63), -8), (dict(B=0), -9), (dict(ldb=31), -10),
+    (dict(C=0), -12), (dict(ldc=10), -13), (dict(mode=3), -14), (dict(mode=-1), -14),
+    (dict(transa="T", lda=31), -8), (dict(transb="T", ldb=47), -10), (dict(lda=0, m=0, transa="N"), -8),
+])
+def test_invalid_arguments_rejected_before_device_work(lib, kw, code):
+    assert _call(lib, _with(**kw)) == code
+    assert "argument %d" % -code in pg.last_error()
+
+
+def test_argument_order_is_signature_order(lib):
+    # both transa and m are bad: the first in signature order is reported
+    assert _call(lib, _with(transa="Z", m=-1)) == -1
+    assert _call(lib, _with(lda=1, ldc=1)) == -8
+
+
+def test_null_pointers_allowed_when_unused(lib):
+    # alpha == 0 with beta == 1: nothing is read or written, so nulls are fine
+    # and the call returns before touching any device.
+    assert _call(lib, _with(A=0, B=0, C=0, alpha=0.0, beta=1.0)) == 0
+    assert _call(lib, _with(m=0, A=0, B=0, C=0)) == 0
+    assert _call(lib, _with(n=0, A=0, B=0, C=0)) == 0
+
+
+def test_python_binding_raises(lib):
+    with pytest.raises(pg.SgemmError) as e:
+        pg.sgemm("N", "N", 4, 4, 4, 1.0, 4096, 2, 4096, 4, 0.0, 4096, 4, "ffma", stream=0)
+    assert e.value.code == -8
+
+
+def plan(m, n, k, mode="ffma", transa="N", transb="N", lda=None, ldb=None, ldc=None, A=1 << 20, B=1 << 21,
+         C=1 << 22, alpha=1.0, beta=0.0, sms=152):
+    ra = m if transa == "N" else k
+    rb = k if transb == "N" else n
+    return pg.sgemm_plan(transa, transb, m, n, k, alpha, A, lda or max(ra, 1), B, ldb or max(rb, 1), beta, C,
+                         ldc or max(m, 1), mode, num_sms=sms)
+
+
+def test_plan_square_uses_wide_tiles_and_no_split(lib):
+    for mode in ("ffma", "tf32", "3xtf32"):
+        p = plan(8192, 8192, 8192, mode)
+        assert p["bn"] == 256 and p["split_k"] == 1 and p["tiles_m"] == 64 and p["tiles_n"] == 32
+        assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc")
+    assert plan(8192, 8192, 8192, "ffma")["prep_a_name"] == "none"
+    assert plan(8192, 8192, 8192, "3xtf32")["prep_a_name"] == "split"
+    assert plan(8192, 8192, 8192, "3xtf32")["launches"] == 3
+
+
+def test_plan_skinny_k_uses_deterministic_split(lib):
+    p = plan(128, 128, 262144, "ffma")
+    assert p["bn"] == 128 and p["tiles_m"] * p["tiles_n"] == 1
+    assert p["split_k"] > 100 and p["split_k"] * p["k_blocks_per_split"] >= p["k_blocks"]
+    assert (p["split_k"] - 1) * p["k_blocks_per_split"] < p["k_blocks"]  # no empty slice
+    assert p["launches"] == 2 and p["workspace_bytes"] >= p["split_k"] * 128 * 128 * 4
+    tall = plan(8192, 64, 8192, "tf32")
+    assert tall["bn"] == 64 and tall["tiles_m"] == 64 and tall["split_k"] == 2
+
+
+def test_plan_misaligned_ld_copies_operand(lib):
+    p = plan(3000, 1500, 777, "ffma", lda=3013, ldb=784, ldc=3005)
+    assert p["prep_a_name"] == "copy" and p["prep_b_name"] == "none"
+    assert p["ld_a"] % 4 == 0 and p["ld_b"] == 784
+    p2 = plan(64, 64, 64, "tf32", A=(1 << 20) + 4)  # base not 16-byte aligned
+    assert p2["prep_a_name"] == "copy"
+
+
+def test_plan_transposed_operands(lib):
+    p = plan(300, 200, 100, "ffma", transa="T", transb="T")
+    assert p["prep_a_name"] == "transpose" and p["prep_b_name"] == "transpose"
+    assert p["ld_a"] == 300 and p["ld_b"] == 100
+
+
+def test_plan_trivial_cases(lib):
+    assert plan(0, 10, 10)["kernel_name"] == "none"
+    assert plan(10, 10, 0, beta=0.5)["kernel_name"] == "scale"
+    assert plan(10, 10, 10, alpha=0.0, beta=1.0)["kernel_name"] == "none"
+
+
+def test_force_plan(lib):
+    try:
+        pg.force_plan(64, 7)
+        p = plan(1024, 1024, 4096)
+        assert p["bn"] == 64 and p["split_k"] == 7
+        with pytest.raises(pg.SgemmError):
+            pg.force_plan(96, 0)
+    finally:
+        pg.force_plan(0, 0)
+
+
+def test_plan_struct_layout_matches_header(lib, tmp_path):
+    """The ctypes mirror of sgemm_plan_t has the C struct's size and offsets."""
+    fields = [f for f, _ in pg.sgemm_plan_t._fields_]
+    src = tmp_path / "layout.c"
+    body = "".join('printf("%%s %%zu\\n", "%s", offsetof(sgemm_plan_t, %s));' % (f, f) for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "precision_gemm.h"\nint main(void){'
+                   + body + 'printf("size %zu\\n", sizeof(sgemm_plan_t)); return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split("\n")
+               if line)
+    for f in fields:
+        assert int(out[f]) == getattr(pg.sgemm_plan_t, f).offset, f
+    assert int(out["size"]) == ctypes.sizeof(pg.sgemm_plan_t)

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Tolerance on the normalised error |C - Cref| / (sum_p |alpha a b| + |beta c|):
+1e-5 for FFMA and 3xTF32, 5e-3 for TF32.  Integer-valued inputs must match
+bit for bit in every mode.  Every run also checks that the leading-dimension
+gaps of C and guard words around every buffer are unchanged.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_gemm_gb300 as pg
+from precision_gemm_gb300 import synth
+from tests import _harness as H
+from tests._golden import colmajor_storage, load_worked
+
+pytestmark = pytest.mark.gpu
+MODES = ("ffma", "tf32", "3xtf32")
+CFG = synth.config_problems()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pg.load_library()
+    pg.force_plan(0, 0)
+    yield
+    pg.force_plan(0, 0)
+    assert pg.device_status() == 0
+
+
+def _assert_ok(res, what):
+    assert res["ok"], "%s: %d/%d entries above tol %.0e (max err %.3e)" % (
+        what, res["n_bad"], res["n"], res["tol"], res["max_err"])
+    assert res["canaries"], "%s: guard words around a buffer changed" % what
+    assert res["padding"], "%s: the ld gap of C changed" % what
+
+
+# ------------------------------------------------------------ the five workloads
+
+@pytest.mark.parametrize("mode", MODES)
+def test_config1_256_full(mode):
+    _assert_ok(H.check_problem(CFG["c1_256"], mode), "256^3 " + mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_config2_rowmajor_1024_full(mode):
+    _assert_ok(H.check_problem(CFG["c2_rm1024"], mode), "row-major 1024^3 " + mode)
+
+
+@pytest.mark.parametrize("size", (2048, 4096))
+@pytest.mark.parametrize("mode", MODES)
+def test_config2_rowmajor_sampled(mode, size):
+    _assert_ok(H.check_problem(CFG["c2_rm%d" % size], mode, sample=4096), "row-major %d^3 %s" % (size, mode))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_config3_ragged_full(mode):
+    _assert_ok(H.check_problem(CFG["c3_ragged"], mode), "ragged 3000x1500x777 " + mode)
+
+
+@pytest.mark.parametrize("mode", ("ffma", "3xtf32", "tf32"))
+def test_config4_8192_sampled(mode):
+    _assert_ok(H.check_problem(CFG["c4_8192"], mode, sample=4096), "8192^3 " + mode)
+
+
+@pytest.mark.parametrize("mode", ("ffma", "3xtf32"))
+def test_config4_16384_sampled(mode):
+    _assert_ok(H.check_problem(CFG["c4_16384"], mode, sample=4096), "16384^3 " + mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_config5a_k64_sampled(mode):
+    _assert_ok(H.check_problem(CFG["c5a_16384x16384x64"], mode, sample=4096), "16384^2x64 " + mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_config5b_splitk_full(mode):
+    p = CFG["c5b_128x128x262144"]
+    plan = pg.sgemm_plan(p.transa, p.transb, p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256,
+                         p.ldc, mode)
+    assert plan["split_k"] > 1, plan
+    _assert_ok(H.check_problem(p, mode), "128x128x262144 " + mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_config5c_tall_thin_sampled(mode):
+    _assert_ok(H.check_problem(CFG["c5c_8192x64x8192"], mode, sample=4096), "8192x64x8192 " + mode)
+
+
+# ------------------------------------------------------------ exactness and structure
+
+@pytest.mark.parametrize("mode", MODES)
+def test_worked_example_exact(mode):
+    """The hand-worked 2x3x2 product of tests/golden, bit for bit."""
+    w = load_worked()
+    m, n, k = w["m"], w["n"], w["k"]
+    for alpha, beta, exp in w["cases"]:
+        A = torch.from_numpy(colmajor_storage(w["opA"], m + 1))
+        B = torch.from_numpy(colmajor_storage(w["opB"], k + 1))
+        C = torch.from_numpy(colmajor_storage(w["Cin"], m + 1))
+        p = synth.Problem(m, n, k, lda=m + 1, ldb=k + 1, ldc=m + 1, alpha=alpha, beta=beta)
+        out, ok = H.run_gpu(p, mode, A, B, C)
+        assert ok and np.array_equal(H.logical(p, out), exp), (mode, alpha, beta, H.logical(p, out))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(300, 260, 1000), (129, 257, 64), (640, 96, 4096)])
+def test_integer_inputs_bitwise(mode, shape):
+    """Integers in [-8, 8]: every product and partial sum is exact in FP32 and in
+    TF32 (11-bit integers are representable), so every mode must agree with the
+    oracle bit for bit, whatever the summation order."""
+    m, n, k = shape
+    p = synth.Problem(m, n, k, lda=m + 3, ldb=k, ldc=m + 1, alpha=1.0, beta=1.0, dist="int", seed=5)
+    A, B, C = synth.make(p)
+    out, ok = H.run_gpu(p, mode, A, B, C)
+    cref, _ = H.reference_full(p, A, B, C)
+    assert ok and H.padding_intact(p, out, C)
+    assert np.array_equal(H.logical(p, out), cref)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_deterministic(mode):
+    """Two runs give bitwise identical C, split-K included."""
+    for p in (CFG["c3_ragged"], CFG["c5b_128x128x262144"].with_(k=65536)):
+        A, B, C = synth.make(p)
+        o1, _ = H.run_gpu(p, mode, A, B, C)
+        o2, _ = H.run_gpu(p, mode, A, B, C)
+        assert torch.equal(o1.view(torch.int32), o2.view(torch.int32)), (p, mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("trans", ["NT", "TN", "TT", "tc"])
+def test_transposed_operands(mode, trans):
+    p = synth.Problem(333, 222, 181, transa=trans[0], transb=trans[1], alpha=0.5, beta=2.0,
+                      dist="normal", seed=7)
+    p = p.with_(lda=p.lda + 5, ldb=p.ldb + 3, ldc=p.ldc + 2)
+    _assert_ok(H.check_problem(p, mode), "trans %s %s" % (trans, mode))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
+                                 (128, 256, 32), (257, 513, 1031), (64, 64, 200000)])
+def test_ragged_and_small(mode, mnk):
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, lda=m + 1, ldb=k + 2, ldc=m + 3, alpha=1.25, beta=-0.75, dist="normal", seed=11)
+    _assert_ok(H.check_problem(p, mode), "%s %s" % (mnk, mode))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_forced_split_and_tiles(mode):
+    p = synth.Problem(300, 200, 2000, alpha=1.0, beta=0.5, dist="normal", seed=13)
+    try:
+        for bn, split in ((64, 3), (128, 5), (256, 2), (64, 1)):
+            pg.force_plan(bn, split)
+            _assert_ok(H.check_problem(p, mode), "bn=%d split=%d %s" % (bn, split, mode))
+    finally:
+        pg.force_plan(0, 0)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_beta_zero_ignores_nan_c(mode):
+    p = synth.Problem(200, 150, 100, alpha=1.0, beta=0.0, dist="normal", seed=17)
+    A, B, C = synth.make(p)
+    C.view(torch.int32).fill_(synth.NAN_BITS)
+    out, ok = H.run_gpu(p, mode, A, B, C)
+    cref, den = H.reference_full(p, A, B, C)
+    assert ok and np.all(np.isfinite(H.logical(p, out)))
+    assert oracle.check(H.logical(p, out), cref, den, oracle.TOL[mode])["ok"]
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_alpha_zero_and_k_zero(mode):
+    p = synth.Problem(70, 50, 30, alpha=0.0, beta=-2.0, dist="normal", seed=19)
+    A, B, C = synth.make(p)
+    A.fill_(float("nan"))
+    B.fill_(float("nan"))
+    out, ok = H.run_gpu(p, mode, A, B, C)
+    assert ok and np.array_equal(H.logical(p, out), -2.0 * H.logical(p, C))
+    pk = p.with_(alpha=1.0, beta=0.0, k=0, ldb=1)
+    out0, _ = H.run_gpu(pk, mode, A[:1], B[:50], C)
+    assert np.all(H.logical(pk, out0) == 0.0)
+    # beta == 1 with nothing to add leaves C untouched
+    out1, _ = H.run_gpu(p.with_(beta=1.0), mode, A, B, C)
+    assert torch.equal(out1.view(torch.int32), C.view(torch.int32))
+
+
+def test_empty_sizes_are_no_ops():
+    C = torch.full((16,), 3.0, device="cuda")
+    pg.sgemm("N", "N", 0, 4, 4, 1.0, None, 1, None, 4, 0.0, C, 1)
+    pg.sgemm("N", "N", 4, 0, 4, 1.0, None, 4, None, 4, 0.0, C, 4)
+    torch.cuda.synchronize()
+    assert torch.all(C == 3.0)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_host_buffers_match_device_path(mode):
+    p = synth.Problem(517, 389, 263, lda=520, ldb=270, ldc=530, alpha=0.75, beta=1.5, dist="normal", seed=23)
+    A, B, C = synth.make(p)
+    dev_out, _ = H.run_gpu(p, mode, A, B, C)
+    Ch = C.clone().pin_memory()
+    pg.sgemm_host("N", "N", p.m, p.n, p.k, p.alpha, A.pin_memory(), p.lda, B.pin_memory(), p.ldb, p.beta, Ch,
+                  p.ldc, mode)
+    assert torch.equal(Ch.view(torch.int32), dev_out.view(torch.int32))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_launch_counter_counts_kernels(mode):
+    for p in (synth.Problem(256, 256, 256), synth.Problem(4096, 4096, 512)):
+        A, B, C = synth.make(p)
+        plan = pg.sgemm_plan("N", "N", p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode,
+                             num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+        before = pg.launch_count()
+        H.run_gpu(p, mode, A, B, C)
+        assert pg.launch_count() - before == plan["launches"]
+
+
+# ------------------------------------------------------------ failure detection
+
+@pytest.mark.parametrize("mode", MODES)
+def test_bounded_wait_reports_timeout(mode):
+    """The operand loader is told to issue nothing, so every other wait in the
+    CTA runs out after the (short) limit; the kernel records SGEMM_ERR_TIMEOUT,
+    exits cleanly, and the context stays usable for the next call."""
+    p = synth.Problem(256, 256, 256, seed=3)
+    A, B, C = synth.make(p)
+    assert pg.device_status() == 0
+    old = pg.set_wait_timeout(20_000_000)  # 20 ms
+    pg.debug_flags(pg.SGEMM_DEBUG_STALL_PRODUCER)
+    try:
+        H.run_gpu(p, mode, A, B, C)
+    finally:
+        pg.debug_flags(0)
+        pg.set_wait_timeout(old)
+    assert pg.device_status(clear=True) == pg.SGEMM_ERR_TIMEOUT
+    assert pg.device_status() == 0
+    _assert_ok(H.check_problem(p, mode), "after a timeout " + mode)
