@@ -40,6 +40,8 @@ WORKLOADS = {
                    synth.Problem(8192, 8192, 8192, alpha=1.0, beta=1.0, dist="uniform", seed=0)),
     "square16384": ("sgemm column-major NN 16384^3, alpha=1 beta=1, A,B,Cin ~ U[-1,1) seed 0",
                     synth.Problem(16384, 16384, 16384, alpha=1.0, beta=1.0, dist="uniform", seed=0)),
+    "square4096": ("sgemm column-major NN 4096^3, alpha=1 beta=1, A,B,Cin ~ U[-1,1) seed 0",
+                   synth.Problem(4096, 4096, 4096, alpha=1.0, beta=1.0, dist="uniform", seed=0)),
     "rowmajor4096": ("sgemm row-major 4096^3, alpha=1 beta=0, A,B ~ U[-1,1) seed 0",
                      synth.Problem(4096, 4096, 4096, alpha=1.0, beta=0.0, dist="uniform", seed=0, layout="row")),
     "ragged": ("sgemm column-major 3000x1500x777, lda=3013 ldb=784 ldc=3005, alpha=1.5 beta=-0.5, N(0,1)",
