@@ -63,6 +63,8 @@ extern "C" {
 #define SGEMM_ERR_TENSOR_MAP 6 /* a TMA tensor map could not be encoded         */
 #define SGEMM_ERR_CAPTURE 7    /* workspace must grow while the stream is being
                                   captured into a CUDA graph                    */
+#define SGEMM_ERR_SCRATCH 8    /* sgemm_noalloc: the call needs more scratch than
+                                  its fixed device array holds                  */
 
 /* Kernel families reported by sgemm_plan(). */
 #define SGEMM_KERNEL_NONE 0    /* nothing to do (m == 0, n == 0, or C unchanged) */
@@ -120,6 +122,39 @@ int sgemm(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha
 int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
                const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                float *C, int64_t ldc, int mode, void *stream);
+
+/*
+ * sgemm_noalloc -- sgemm without any device allocation.  (The pages have no
+ * counterpart: this entry exists for callers of this library, not for the
+ * method.)
+ *
+ * Who needs it: callers that cannot call cudaMalloc -- a process in which
+ * another allocator has reserved the device memory up front, or a
+ * latency-critical loop in which cudaMalloc/cudaFree, which may synchronise
+ * the device, are not allowed.  sgemm itself may allocate its workspace on
+ * first use of a size; this call never does.  Its only scratch, the split-K
+ * partial sums, lives in a fixed 16 MiB array in device memory that every
+ * GPU loading the library holds until the process exits.
+ *
+ * Arguments are those of sgemm, with these limits: mode is SGEMM_FFMA or
+ * SGEMM_TF32 (else -14); transa and transb are 'N' (else -1, -2); A and B are
+ * 16-byte aligned with lda and ldb multiples of 4 (else -7/-8, -9/-10), so the
+ * kernels read them in place; and the call's split-K partial sums,
+ * split_k * round_up(m, 4) * n * 4 bytes as sgemm_plan reports split_k, fit in
+ * the 16 MiB array (else SGEMM_ERR_SCRATCH, and nothing is launched).  Results
+ * equal sgemm's for the same arguments.
+ *
+ * The first call on a device takes the array's device address (a
+ * cudaGetSymbolAddress call with that device current, done once per device);
+ * make that first call before any stream capture.  Every call shares the one
+ * array and leaves its contents behind; each call writes every partial sum
+ * before reading it, so nothing needs clearing, but calls whose work overlaps
+ * on the GPU (different streams, or different host threads) race on the array
+ * and must be serialised by the caller.
+ */
+int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+                  const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                  float *C, int64_t ldc, int mode, void *stream);
 
 /* The choices sgemm would make for a call (see sgemm_plan). */
 typedef struct sgemm_plan {

@@ -27,14 +27,15 @@ MODES = {"ffma": SGEMM_FFMA, "tf32": SGEMM_TF32, "3xtf32": SGEMM_3XTF32}
 MODE_NAMES = {v: k for k, v in MODES.items()}
 
 SGEMM_ERR = {1: "SGEMM_ERR_CUDA", 2: "SGEMM_ERR_NO_DEVICE", 3: "SGEMM_ERR_ARCH", 4: "SGEMM_ERR_TIMEOUT",
-             5: "SGEMM_ERR_ALLOC", 6: "SGEMM_ERR_TENSOR_MAP", 7: "SGEMM_ERR_CAPTURE"}
+             5: "SGEMM_ERR_ALLOC", 6: "SGEMM_ERR_TENSOR_MAP", 7: "SGEMM_ERR_CAPTURE", 8: "SGEMM_ERR_SCRATCH"}
+SGEMM_ERR_SCRATCH = 8
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_DEBUG_STALL_PRODUCER = 1
 KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc"}
 PREPS = {0: "none", 1: "copy", 2: "transpose", 3: "split"}
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTS = ("sgemm", "sgemm_host", "sgemm_plan", "sgemm_device_status", "sgemm_set_wait_timeout",
+EXPORTS = ("sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_plan", "sgemm_device_status", "sgemm_set_wait_timeout",
            "sgemm_force_plan", "sgemm_debug_flags", "sgemm_launch_count", "sgemm_workspace_release",
            "sgemm_last_error_string", "sgemm_version")
 
@@ -77,6 +78,8 @@ def load_library(path: str | None = None):
         lib.sgemm.restype = i
         lib.sgemm_host.argtypes = gemm_args
         lib.sgemm_host.restype = i
+        lib.sgemm_noalloc.argtypes = gemm_args
+        lib.sgemm_noalloc.restype = i
         lib.sgemm_plan.argtypes = gemm_args[:14] + [i, ctypes.POINTER(sgemm_plan_t)]
         lib.sgemm_plan.restype = i
         lib.sgemm_device_status.argtypes = [vp, i]
@@ -148,6 +151,18 @@ def sgemm_host(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mod
     lib = load_library()
     _check(lib.sgemm_host(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                           _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
+
+
+def sgemm_noalloc(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma",
+                  stream=None) -> None:
+    """sgemm for callers that cannot allocate device memory: never calls cudaMalloc;
+    its split-K scratch is a fixed 16 MiB device array shared by every call (calls
+    that overlap on the GPU race on it).  FFMA or TF32, untransposed 16-byte
+    aligned operands with ld multiples of 4; raises SgemmError (code
+    SGEMM_ERR_SCRATCH) when the call's partial sums would not fit."""
+    lib = load_library()
+    _check(lib.sgemm_noalloc(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                             _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
 
 
 def sgemm_rm(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma", stream=None) -> None:

@@ -398,6 +398,113 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     return 0;
 }
 
+// ---- the allocation-free variant (sgemm_noalloc) ---------------------------------------
+//
+// Callers that cannot call cudaMalloc -- a process whose device memory is all
+// reserved up front by another allocator, or a latency-critical loop in which
+// cudaMalloc/cudaFree (which may synchronise the device) are not allowed -- get
+// one entry point whose only scratch, the split-K partial sums, lives in this
+// fixed array.  Every GPU that loads the library holds the array until the
+// process exits.  Host code cannot use the array's name as a device address (it
+// names a host-side stand-in), so each device's address is taken once with
+// cudaGetSymbolAddress while that device is current.
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+float* g_noalloc_ptr[kMaxDevices];  // device address of the array, per device (guarded by g_dev_mu)
+
+int noalloc_scratch(int dev, float** out) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        float* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(no-allocation scratch)");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return 0;
+}
+
+int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
+                int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
+                cudaStream_t st) {
+    if (mode != SGEMM_FFMA && mode != SGEMM_TF32)
+        return fail(-14, "argument 14 (mode): sgemm_noalloc supports SGEMM_FFMA and SGEMM_TF32 only (3xTF32 needs "
+                         "split operands in a workspace)");
+    if (!is_notrans(transa)) return fail(-1, "argument 1 (transa): sgemm_noalloc reads A untransposed ('N')");
+    if (!is_notrans(transb)) return fail(-2, "argument 2 (transb): sgemm_noalloc reads B untransposed ('N')");
+    if (!aligned16(A)) return fail(-7, "argument 7 (A): sgemm_noalloc needs a 16-byte aligned A");
+    if (lda % 4 != 0) return fail(-8, "argument 8 (lda): sgemm_noalloc needs lda to be a multiple of 4");
+    if (!aligned16(B)) return fail(-9, "argument 9 (B): sgemm_noalloc needs a 16-byte aligned B");
+    if (ldb % 4 != 0) return fail(-10, "argument 10 (ldb): sgemm_noalloc needs ldb to be a multiple of 4");
+    int dev;
+    DeviceState* ds;
+    int rc = current_device(&dev, &ds);
+    if (rc) return rc;
+    sgemm_plan_t pl;
+    make_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, mode, ds->sms, &pl);
+    cudaError_t e;
+    if (pl.kernel == SGEMM_KERNEL_NONE) return 0;
+    if (pl.kernel == SGEMM_KERNEL_SCALE) {
+        if ((e = launch_scale(C, ldc, m, n, beta, ds->sms, st)) != cudaSuccess) return fail_cuda(e, "scale kernel");
+        g_launches += 1;
+        return 0;
+    }
+    const int64_t ldp = round_up(m, 4);
+    const size_t need = pl.split_k > 1 ? static_cast<size_t>(pl.split_k) * ldp * n * sizeof(float) : 0;
+    if (need > kNoAllocScratchBytes)
+        return fail(SGEMM_ERR_SCRATCH,
+                    "sgemm_noalloc: %d K slices of a %lld x %lld result need %zu bytes of scratch; the fixed device "
+                    "array holds %zu bytes",
+                    pl.split_k, (long long)m, (long long)n, need, kNoAllocScratchBytes);
+    float* scratch = nullptr;
+    if ((rc = noalloc_scratch(dev, &scratch))) return rc;
+
+    GemmParams gp{};
+    gp.m = m;
+    gp.n = n;
+    gp.k = k;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.C = C;
+    gp.ldc = ldc;
+    gp.split = pl.split_k;
+    if (pl.split_k > 1) {
+        gp.P = scratch;  // every partial read by the reduction is written first: nothing to clear
+        gp.ldp = ldp;
+        gp.p_stride = ldp * n;
+    }
+    gp.tiles_m = pl.tiles_m;
+    gp.tiles_n = pl.tiles_n;
+    gp.kb_total = pl.k_blocks;
+    gp.kb_per_split = pl.k_blocks_per_split;
+    gp.group_m = 16;
+    gp.c_vec = aligned16(C) && (ldc % 4 == 0);
+    gp.debug_flags = g_debug.load();
+    gp.timeout_ns = g_timeout_ns.load();
+    gp.status = ds->status;
+
+    const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
+    CUtensorMap tmA, tmB;
+    if (pl.kernel == SGEMM_KERNEL_FFMA) {
+        if ((rc = encode_2d(&tmA, A, m, k, lda, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
+        if ((rc = encode_2d(&tmB, B, k, n, ldb, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+        if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");
+    } else {
+        if ((rc = encode_2d(&tmA, A, m, k, lda, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))) return rc;
+        if ((rc = encode_2d(&tmB, B, k, n, ldb, pl.bk, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+        if ((e = launch_tc(tmA, tmA, tmB, tmB, gp, pl.bn, false, grid, st)) != cudaSuccess)
+            return fail_cuda(e, "tcgen05 GEMM kernel");
+    }
+    if (pl.split_k > 1) {
+        if ((e = launch_splitk_reduce(gp, ds->sms, st)) != cudaSuccess) return fail_cuda(e, "split-K reduction");
+    }
+    g_launches += pl.launches;
+    return 0;
+}
+
 }  // namespace
 }  // namespace pg
 
@@ -453,6 +560,16 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
         return fail_cuda(e, "copy of C to the host");
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
     return 0;
+}
+
+PG_EXPORT int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+                            const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc, int mode, void* stream) {
+    int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
+    if (rc) return rc;
+    if (m == 0 || n == 0 || ((k == 0 || alpha == 0.0f) && beta == 1.0f)) return 0;  // C unchanged
+    return run_noalloc(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode,
+                       static_cast<cudaStream_t>(stream));
 }
 
 PG_EXPORT int sgemm_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,
