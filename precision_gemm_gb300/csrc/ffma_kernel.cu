@@ -35,6 +35,13 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+// PG_FFMA_PACKED selects the packed two-lane FP32 FMA (fma.rn.f32x2, sm_100+):
+// one instruction updates a pair of accumulators (two rows of one column) with
+// the A pair of those rows and the B value of the column.
+#ifndef PG_FFMA_PACKED
+#define PG_FFMA_PACKED 1
+#endif
+
 namespace pg {
 namespace {
 
@@ -72,8 +79,7 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
     using Cfg = FfmaCfg<BN>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S);
     const uint32_t full0 = smem_u32(bars);
@@ -133,11 +139,13 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
     const int tn = 8 * wn + (lane & 7);    // 0..TGN-1
     const uint32_t bchunk_xor = static_cast<uint32_t>(tn & 7);
 
-    float acc[8][8];
+    // acc[r][jj] holds rows (2r, 2r+1) of the thread's 8 rows {4tm..4tm+3, 64+4tm..64+4tm+3}
+    // in column jj, as a register pair (the operand shape of the packed FP32 FMA).
+    float2 acc[4][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < 8; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
 
     bool ok = true;
     for (int it = 0; it < nkb; ++it) {
@@ -167,11 +175,21 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
                 const float* arow = As + (4 * g + kk) * Cfg::BM;
                 const float4 a0 = *reinterpret_cast<const float4*>(arow + 4 * tm);
                 const float4 a1 = *reinterpret_cast<const float4*>(arow + 64 + 4 * tm);
-                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float2 a[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                                     make_float2(a1.z, a1.w)};
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int jj = 0; jj < 8; ++jj) {
+                    const float bv = comp(b[jj], kk);
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) acc[i][jj] = fmaf(a[i], comp(b[jj], kk), acc[i][jj]);
+                    for (int r = 0; r < 4; ++r) {
+#if PG_FFMA_PACKED
+                        acc[r][jj] = __ffma2_rn(a[r], make_float2(bv, bv), acc[r][jj]);
+#else
+                        acc[r][jj].x = fmaf(a[r].x, bv, acc[r][jj].x);
+                        acc[r][jj].y = fmaf(a[r].y, bv, acc[r][jj].y);
+#endif
+                    }
+                }
             }
         }
         __syncwarp();
@@ -195,7 +213,7 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
         for (int h = 0; h < 2; ++h) {
             const int64_t i = m0 + 64 * h + 4 * tm;
             if (i >= p.m) continue;
-            const float v[4] = {acc[4 * h][jj], acc[4 * h + 1][jj], acc[4 * h + 2][jj], acc[4 * h + 3][jj]};
+            const float v[4] = {acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y};
             if (p.split > 1) {
                 float* dst = p.P + slice * p.p_stride + j * p.ldp + i;
                 if (i + 3 < p.m) {

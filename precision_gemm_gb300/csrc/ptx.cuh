@@ -15,6 +15,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to 1 KiB (the 128-byte swizzle
+// atom).  The offset is added to the __shared__ array itself so the compiler
+// keeps the shared address space: loads through the result are ld.shared with
+// 32-bit addresses, not generic loads.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* base) {
+    return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -78,8 +78,7 @@ __global__ void __launch_bounds__(192, 1)
     using Cfg = TcCfg<BN, SPLIT3>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
