@@ -19,13 +19,21 @@
 //     lands as BN rows of 32 floats (128 B) with the 128-byte TMA swizzle, so a
 //     quarter-warp reading one 16-byte chunk from 8 different rows hits 8
 //     different bank groups (no bank conflicts, the wiki's V3.1/V3.2 goal);
-//   * each consumer thread owns an 8 x 8 register tile: rows {4tm..4tm+3} and
-//     {64+4tm..64+4tm+3}, columns {tn + (BN/8)*jj}; per group of 4 k values it
-//     reads 8 float4 of B (4 k values of one column each) and 2 float4 of A per
-//     k, then issues 256 FMAs;
+//   * each thread owns an 8 x 8 register tile: rows {4tm..4tm+3} and
+//     {64+4tm..64+4tm+3}, columns {tn + (BN/8)*jj}, held as 4 x 8 register
+//     pairs (two rows of one column).  Per pair of k values it reads 8 float2
+//     of B (two k values of one column each) and, per k, 2 float4 of A, then
+//     issues 32 packed two-lane FMAs (fma.rn.f32x2, sm_100 and later: the A
+//     pair of two rows times the broadcast B value of the column), which halves
+//     the FMA instructions that compete for issue slots;
 //   * the epilogue computes alpha*acc + beta*C in registers and stores float4s
 //     (scalar stores at ragged edges or when C / ldc is not 16-byte aligned);
 //     with split-K it writes raw partial sums instead.
+//
+// Tile shapes: 128 x 128 (256 threads, 3 slots, two CTAs per SM) is the default;
+// 128 x 64 serves n <= 64 and 128 x 256 (512 threads, 4 slots) stays selectable.
+// Measured on GB300 at 8192^3: 128 x 128 with float2 B reads and PD = 1 runs at
+// 62.7 TFLOP/s against 58.7 for 128 x 256 with float4 B reads.
 //
 // Every mbarrier wait is bounded (see ptx.cuh); a CTA whose wait expires marks
 // the device status word, waits (bounded) for its own TMA copies and exits.
@@ -34,13 +42,6 @@
 
 #include "internal.h"
 #include "ptx.cuh"
-
-// PG_FFMA_PACKED selects the packed two-lane FP32 FMA (fma.rn.f32x2, sm_100+):
-// one instruction updates a pair of accumulators (two rows of one column) with
-// the A pair of those rows and the B value of the column.
-#ifndef PG_FFMA_PACKED
-#define PG_FFMA_PACKED 1
-#endif
 
 namespace pg {
 namespace {
@@ -57,7 +58,7 @@ struct FfmaCfg {
     // (it + PD) % STAGES, whose previous contents (k-block it + PD - STAGES) every
     // warp released STAGES - PD iterations ago; with a spare slot (PD = STAGES-2)
     // the loader waits only if some warp trails by two whole k-blocks.
-    static constexpr int PD = (STAGES >= 4) ? STAGES - 2 : STAGES - 1;
+    static constexpr int PD = STAGES - 2;
     static constexpr int CTAS_PER_SM = (BN == 256) ? 1 : 2;
     static constexpr int A_BYTES = BM * BK * 4;           // 16 KiB
     static constexpr int B_BYTES = BN * BK * 4;           // BN rows of 128 B
@@ -164,31 +165,24 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
         const float* As = reinterpret_cast<const float*>(smem + s * Cfg::STAGE_BYTES);
         const uint8_t* Bs = smem + s * Cfg::STAGE_BYTES + Cfg::A_BYTES + tn * 128;
 #pragma unroll
-        for (int g = 0; g < Cfg::BK / 4; ++g) {
-            float4 b[8];
-            const uint32_t chunk = (static_cast<uint32_t>(g) ^ bchunk_xor) << 4;
+        for (int g2 = 0; g2 < Cfg::BK / 2; ++g2) {
+            float2 b[8];
+            const uint32_t off2 = (((static_cast<uint32_t>(g2 >> 1)) ^ bchunk_xor) << 4) + ((g2 & 1) << 3);
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj)
-                b[jj] = *reinterpret_cast<const float4*>(Bs + jj * (Cfg::TGN * 128) + chunk);
+                b[jj] = *reinterpret_cast<const float2*>(Bs + jj * (Cfg::TGN * 128) + off2);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float* arow = As + (4 * g + kk) * Cfg::BM;
+            for (int kk = 0; kk < 2; ++kk) {
+                const float* arow = As + (2 * g2 + kk) * Cfg::BM;
                 const float4 a0 = *reinterpret_cast<const float4*>(arow + 4 * tm);
                 const float4 a1 = *reinterpret_cast<const float4*>(arow + 64 + 4 * tm);
                 const float2 a[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
                                      make_float2(a1.z, a1.w)};
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
-                    const float bv = comp(b[jj], kk);
+                    const float bv = kk == 0 ? b[jj].x : b[jj].y;
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-#if PG_FFMA_PACKED
-                        acc[r][jj] = __ffma2_rn(a[r], make_float2(bv, bv), acc[r][jj]);
-#else
-                        acc[r][jj].x = fmaf(a[r].x, bv, acc[r][jj].x);
-                        acc[r][jj].y = fmaf(a[r].y, bv, acc[r][jj].y);
-#endif
-                    }
+                    for (int r = 0; r < 4; ++r) acc[r][jj] = __ffma2_rn(a[r], make_float2(bv, bv), acc[r][jj]);
                 }
             }
         }

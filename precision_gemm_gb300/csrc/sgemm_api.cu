@@ -128,8 +128,9 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->ld_a = pl->prep_a == SGEMM_PREP_NONE ? lda : round_up(m, 4);
     pl->ld_b = pl->prep_b == SGEMM_PREP_NONE ? ldb : round_up(k, 4);
 
-    // Tile width: the narrowest of 64/128/256 that covers n, else 256.
-    int bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
+    // Tile width: 64 for n <= 64; otherwise 128 for the FFMA kernel (two CTAs per
+    // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05.
+    int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
     const int fbn = g_force_bn.load();
     if (fbn) bn = fbn;
     pl->bn = bn;

@@ -110,8 +110,10 @@ def plan(m, n, k, mode="ffma", transa="N", transb="N", lda=None, ldb=None, ldc=N
 def test_plan_square_uses_wide_tiles_and_no_split(lib):
     for mode in ("ffma", "tf32", "3xtf32"):
         p = plan(8192, 8192, 8192, mode)
-        assert p["bn"] == 256 and p["split_k"] == 1 and p["tiles_m"] == 64 and p["tiles_n"] == 32
+        bn = 128 if mode == "ffma" else 256  # FFMA: 128 x 128 tiles, two CTAs per SM
+        assert p["bn"] == bn and p["split_k"] == 1 and p["tiles_m"] == 64 and p["tiles_n"] == 8192 // bn
         assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc")
+        assert p["ctas_per_sm"] == (2 if mode == "ffma" else 1)
     assert plan(8192, 8192, 8192, "ffma")["prep_a_name"] == "none"
     assert plan(8192, 8192, 8192, "3xtf32")["prep_a_name"] == "split"
     assert plan(8192, 8192, 8192, "3xtf32")["launches"] == 3
