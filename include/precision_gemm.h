@@ -70,7 +70,9 @@ extern "C" {
 #define SGEMM_KERNEL_NONE 0    /* nothing to do (m == 0, n == 0, or C unchanged) */
 #define SGEMM_KERNEL_SCALE 1   /* C = beta * C only (k == 0 or alpha == 0)       */
 #define SGEMM_KERNEL_FFMA 2    /* CUDA-core FP32 kernel                         */
-#define SGEMM_KERNEL_TC 3      /* tcgen05 tensor-core kernel                    */
+#define SGEMM_KERNEL_TC 3      /* tcgen05 tensor-core kernel, one SM per tile   */
+#define SGEMM_KERNEL_TC2 4     /* tcgen05 on SM pairs (cta_group::2), 256-row
+                                  tiles, persistent                              */
 
 /* How an operand reaches the GEMM kernel (sgemm_plan_t.prep_a / prep_b). */
 #define SGEMM_PREP_NONE 0      /* read in place through TMA                     */
@@ -160,7 +162,7 @@ int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, flo
 typedef struct sgemm_plan {
     int kernel;              /* SGEMM_KERNEL_*                                  */
     int mode;                /* the mode argument                               */
-    int bm, bn, bk, stages;  /* CTA tile and shared-memory ring depth           */
+    int bm, bn, bk, stages;  /* output tile (bm = 256 on SM pairs), ring depth  */
     int split_k;             /* number of K slices (1: no split)                */
     int k_blocks;            /* BK-sized blocks of K in total                   */
     int k_blocks_per_split;  /* BK-sized blocks each slice reduces              */

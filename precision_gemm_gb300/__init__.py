@@ -31,7 +31,7 @@ SGEMM_ERR = {1: "SGEMM_ERR_CUDA", 2: "SGEMM_ERR_NO_DEVICE", 3: "SGEMM_ERR_ARCH",
 SGEMM_ERR_SCRATCH = 8
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_DEBUG_STALL_PRODUCER = 1
-KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc"}
+KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc", 4: "tc2"}
 PREPS = {0: "none", 1: "copy", 2: "transpose", 3: "split"}
 
 # Every symbol the header declares (checked by the CPU tests).

@@ -15,7 +15,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libprecision_gemm.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["sgemm_api.cu", "ffma_kernel.cu", "tc_kernel.cu", "aux_kernels.cu"]
+SOURCES = ["sgemm_api.cu", "ffma_kernel.cu", "tc_kernel.cu", "tc2_kernel.cu", "aux_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]

@@ -54,6 +54,14 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUt
                       const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3,
                       dim3 grid, cudaStream_t stream);
 
+// tcgen05 kernel on SM pairs (cta_group::2, persistent, double-buffered TMEM):
+// pair tile 256 x bn, bn in {128, 256}; launches min(units, resident pairs) pairs.
+int tc2_stages(int bn, bool split3);
+size_t tc2_smem_bytes(int bn, bool split3);
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
+                       const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3, int units, int num_sms,
+                       cudaStream_t stream, int* pairs_launched);
+
 // Operand preparation: dst(r, c) = src(r, c) (or src(c, r) when transposed) for
 // r < rows, c < cols, dst with leading dimension ldd.  With dst_small != null
 // the value is split into a TF32 "big" part (dst) and the exact remainder

@@ -134,20 +134,26 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     const int fbn = g_force_bn.load();
     if (fbn) bn = fbn;
     pl->bn = bn;
-    pl->kernel = tc ? SGEMM_KERNEL_TC : SGEMM_KERNEL_FFMA;
+    // Tensor-core modes run on SM pairs (256-row tiles, cta_group::2) when m > 128;
+    // a single-SM 128-row tile serves m <= 128 and the 64-wide tile.
+    const bool pair = tc && m > kBM && bn >= 128;
+    pl->kernel = !tc ? SGEMM_KERNEL_FFMA : (pair ? SGEMM_KERNEL_TC2 : SGEMM_KERNEL_TC);
+    pl->bm = pair ? 2 * kBM : kBM;
     pl->bk = tc ? tc_bk(split3) : kFfmaBK;
-    pl->stages = tc ? tc_stages(bn, split3) : ffma_stages(bn);
+    pl->stages = !tc ? ffma_stages(bn) : (pair ? tc2_stages(bn, split3) : tc_stages(bn, split3));
     pl->threads = tc ? tc_threads() : ffma_threads(bn);
     pl->ctas_per_sm = tc ? 1 : ffma_ctas_per_sm(bn);
-    pl->smem_bytes = tc ? tc_smem_bytes(bn, split3) : ffma_smem_bytes(bn);
-    pl->tiles_m = static_cast<int>(cdiv(m, kBM));
+    pl->smem_bytes = !tc ? ffma_smem_bytes(bn) : (pair ? tc2_smem_bytes(bn, split3) : tc_smem_bytes(bn, split3));
+    pl->tiles_m = static_cast<int>(cdiv(m, pl->bm));
     pl->tiles_n = static_cast<int>(cdiv(n, bn));
     pl->k_blocks = static_cast<int>(cdiv(k, pl->bk));
 
     // Split-K when the output tiles cannot fill one wave of the machine: give
-    // each tile floor(capacity / tiles) K slices of at least 4 K blocks each.
+    // each tile floor(capacity / tiles) K slices of at least 4 K blocks each
+    // (capacity counts SM pairs for the pair kernel).
     const int64_t tiles = static_cast<int64_t>(pl->tiles_m) * pl->tiles_n;
-    const int64_t capacity = static_cast<int64_t>(std::max(num_sms, 1)) * pl->ctas_per_sm;
+    const int64_t capacity =
+        pair ? std::max(num_sms / 2, 1) : static_cast<int64_t>(std::max(num_sms, 1)) * pl->ctas_per_sm;
     int64_t split = 1;
     const int fs = g_force_split.load();
     if (fs > 0) {
@@ -294,6 +300,52 @@ int encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, i
     return 0;
 }
 
+// Encode the tensor maps the planned kernel reads, launch it, then the split-K
+// reduction when the plan splits K.  Operands are in the kernels' layout here
+// (A M-major with ld pl.ld_a, B K-major with ld pl.ld_b).
+int launch_gemm(const sgemm_plan_t& pl, bool split3, const float* a_big, const float* a_small, const float* b_big,
+                const float* b_small, int64_t m, int64_t n, int64_t k, GemmParams& gp, int num_sms, cudaStream_t st) {
+    int rc;
+    cudaError_t e;
+    CUtensorMap tmA, tmB, tmAs, tmBs;
+    if (pl.kernel == SGEMM_KERNEL_FFMA) {
+        const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
+        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
+        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+        if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");
+    } else {
+        // tcgen05: A in 32-row boxes (M-major, 32-byte-atom swizzle), B in boxes of
+        // pl.bk x (bn, or bn/2 per CTA on SM pairs).
+        const bool pair = pl.kernel == SGEMM_KERNEL_TC2;
+        const uint32_t b_cols = pair ? pl.bn / 2 : pl.bn;
+        const CUtensorMapSwizzle bsw = pl.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))) return rc;
+        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, pl.bk, b_cols, bsw))) return rc;
+        tmAs = tmA;
+        tmBs = tmB;
+        if (split3) {
+            if ((rc = encode_2d(&tmAs, a_small, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)))
+                return rc;
+            if ((rc = encode_2d(&tmBs, b_small, k, n, pl.ld_b, pl.bk, b_cols, bsw))) return rc;
+        }
+        if (pair) {
+            int pairs = 0;
+            const int units = pl.tiles_m * pl.tiles_n * pl.split_k;
+            if ((e = launch_tc2(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, units, num_sms, st, &pairs)) != cudaSuccess)
+                return fail_cuda(e, "tcgen05 SM-pair GEMM kernel");
+        } else {
+            const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
+            if ((e = launch_tc(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
+                return fail_cuda(e, "tcgen05 GEMM kernel");
+        }
+    }
+    if (pl.split_k > 1) {
+        if ((e = launch_splitk_reduce(gp, num_sms, st)) != cudaSuccess) return fail_cuda(e, "split-K reduction");
+    }
+    g_launches += pl.launches;
+    return 0;
+}
+
 // ---- the call ---------------------------------------------------------------------------
 
 int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
@@ -372,31 +424,7 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     gp.timeout_ns = g_timeout_ns.load();
     gp.status = ds->status;
 
-    const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
-    CUtensorMap tmA, tmB, tmAs, tmBs;
-    if (pl.kernel == SGEMM_KERNEL_FFMA) {
-        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
-        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
-        if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");
-    } else {
-        const CUtensorMapSwizzle bsw = pl.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))) return rc;
-        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, pl.bk, pl.bn, bsw))) return rc;
-        tmAs = tmA;
-        tmBs = tmB;
-        if (split3) {
-            if ((rc = encode_2d(&tmAs, a_small, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)))
-                return rc;
-            if ((rc = encode_2d(&tmBs, b_small, k, n, pl.ld_b, pl.bk, pl.bn, bsw))) return rc;
-        }
-        if ((e = launch_tc(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
-            return fail_cuda(e, "tcgen05 GEMM kernel");
-    }
-    if (pl.split_k > 1) {
-        if ((e = launch_splitk_reduce(gp, ds->sms, st)) != cudaSuccess) return fail_cuda(e, "split-K reduction");
-    }
-    g_launches += pl.launches;
-    return 0;
+    return launch_gemm(pl, split3, a_big, a_small, b_big, b_small, m, n, k, gp, ds->sms, st);
 }
 
 // ---- the allocation-free variant (sgemm_noalloc) ---------------------------------------
@@ -487,23 +515,7 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     gp.timeout_ns = g_timeout_ns.load();
     gp.status = ds->status;
 
-    const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
-    CUtensorMap tmA, tmB;
-    if (pl.kernel == SGEMM_KERNEL_FFMA) {
-        if ((rc = encode_2d(&tmA, A, m, k, lda, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
-        if ((rc = encode_2d(&tmB, B, k, n, ldb, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
-        if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");
-    } else {
-        if ((rc = encode_2d(&tmA, A, m, k, lda, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))) return rc;
-        if ((rc = encode_2d(&tmB, B, k, n, ldb, pl.bk, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
-        if ((e = launch_tc(tmA, tmA, tmB, tmB, gp, pl.bn, false, grid, st)) != cudaSuccess)
-            return fail_cuda(e, "tcgen05 GEMM kernel");
-    }
-    if (pl.split_k > 1) {
-        if ((e = launch_splitk_reduce(gp, ds->sms, st)) != cudaSuccess) return fail_cuda(e, "split-K reduction");
-    }
-    g_launches += pl.launches;
-    return 0;
+    return launch_gemm(pl, false, A, A, B, B, m, n, k, gp, ds->sms, st);
 }
 
 }  // namespace

@@ -1,0 +1,413 @@
+// Tensor-core GEMM on SM pairs (tcgen05 cta_group::2, sm_103a): TF32 and 3xTF32.
+//
+// A cluster of two CTAs on two SMs computes a 256 x BN tile of C per work unit:
+// CTA r of the pair stages rows [128r, 128r + 128) of the A tile and columns
+// [r*BN/2, (r+1)*BN/2) of the B tile, and one thread of CTA 0 issues
+// tcgen05.mma.cta_group::2 (M = 256, N = BN, K = 8), which reads both CTAs'
+// shared memory and leaves rows 128r.. of the product in CTA r's tensor memory.
+// Each SM therefore stages 128 + BN/2 operand rows per k-step instead of
+// 128 + BN, which is what bounds the single-SM kernel (its operand feed, not the
+// tensor pipe, is the limit measured with ncu).
+//
+// The kernel is persistent: each pair walks work units (tile, K slice) with a
+// static stride, and the accumulator is double-buffered in TMEM (2 x BN columns)
+// so the epilogue of one unit overlaps the MMAs of the next.
+//
+// Warp roles, in both CTAs of the pair (192 threads each):
+//   warp 0      TMA loader: this CTA's A rows and B columns for every k-block,
+//               completing on CTA 0's "full" barrier of the ring slot
+//   warp 1      TMEM allocation (pair-wide); in CTA 0 one thread issues the MMAs
+//   warps 2-5   epilogue: TMEM -> registers -> alpha/beta -> C rows of this CTA
+// Barriers: full[s] (CTA 0: expect-tx for both CTAs' bytes), empty[s] (both CTAs;
+// the MMA completion is multicast), acc_full[b] (both CTAs; multicast),
+// acc_empty[b] (CTA 0; arrived by the 8 epilogue warps of the pair).
+//
+// Shared-memory layouts are those of the single-SM kernel (tc_kernel.cu): A
+// M-major in the 128-byte swizzle with 32-byte atoms, B K-major in the 128-byte
+// (BK 32) or 64-byte (BK 16) swizzle.  In the pair the descriptors name
+// offsets that are valid in both CTAs (the slots sit at the same offsets).
+//
+// Every wait is bounded.  After an expired wait a CTA raises its abort flag and
+// the status word, lets the MMAs it issued finish (bounded), and meets its peer
+// at the final cluster barrier before TMEM is released; a peer whose waits
+// then expire in turn leaves the same way.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pg {
+namespace {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA tile load into this CTA's shared memory that completes on the mbarrier at
+// `bar_cluster` (CTA 0 of the pair).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at offset `bar` in both CTAs of the pair once the MMAs
+// issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+// Arrive on this CTA's barrier `bar` once the MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+template <int BN, bool SPLIT3>
+struct Tc2Cfg {
+    static constexpr int BM = kBM;               // rows per CTA (256 per pair)
+    static constexpr int BK = SPLIT3 ? 16 : 32;
+    static constexpr int OPS = SPLIT3 ? 2 : 1;
+    static constexpr int BNH = BN / 2;           // B columns staged per CTA
+    static constexpr int A_BYTES = BM * BK * 4;
+    static constexpr int B_BYTES = BNH * BK * 4;
+    static constexpr int A_BOX_BYTES = 32 * BK * 4;
+    static constexpr int STAGE_BYTES = OPS * (A_BYTES + B_BYTES);
+    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int THREADS = 192;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_tf32(2 * BM, BN, /*a_mn_major=*/true, /*b_mn_major=*/false);
+    static constexpr uint32_t A_LBO = 128 * BK;
+    static constexpr uint32_t A_SBO = 512;
+    static constexpr uint32_t B_SBO = (BK == 32) ? 1024 : 512;
+    static constexpr uint32_t B_LAYOUT = (BK == 32) ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulator buffers
+    static_assert(BN == 128 || BN == 256, "BN");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
+    static_assert(STAGES >= 3, "ring too shallow");
+};
+
+template <int BN, bool SPLIT3>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
+                    const GemmParams p) {
+    using Cfg = Tc2Cfg<BN, SPLIT3>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_smem_1024(smem_raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+    // [0,S) full, [S,2S) empty, 2S..2S+1 acc_full, 2S+2..2S+3 acc_empty, 2S+4 mma_done
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + S);
+    const uint32_t acc_full0 = smem_u32(bars + 2 * S);
+    const uint32_t acc_empty0 = smem_u32(bars + 2 * S + 2);
+    const uint32_t mma_done = smem_u32(bars + 2 * S + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int pairs = gridDim.x >> 1;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int units = tiles * p.split;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full0 + 8 * b, 1);
+            mbar_init(acc_empty0 + 8 * b, 8);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(Cfg::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    // Work unit -> (pair tile, K slice, k-block range).
+    auto unit_geometry = [&](int u, int64_t& m0, int64_t& n0, int& slice, int& kb0, int& nkb) {
+        const int t = u % tiles;
+        slice = u / tiles;
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        m0 = static_cast<int64_t>(tm) * (2 * Cfg::BM);
+        n0 = static_cast<int64_t>(tn) * BN;
+        kb0 = slice * p.kb_per_split;
+        nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
+    };
+
+    if (warp == 0) {
+        // ---------------- TMA loader (both CTAs) ----------------
+        if (lane == 0 && !(p.debug_flags & 1)) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+            if (SPLIT3) {
+                prefetch_tmap(&tmAs);
+                prefetch_tmap(&tmBs);
+            }
+            const uint32_t full_leader0 = map_to_rank(full0, 0);
+            int it = 0;
+            bool ok = true;
+            for (int u = pair; u < units && ok; u += pairs) {
+                int64_t m0, n0;
+                int slice, kb0, nkb;
+                unit_geometry(u, m0, n0, slice, kb0, nkb);
+                const int32_t ma = static_cast<int32_t>(m0 + Cfg::BM * rank);
+                const int32_t nb = static_cast<int32_t>(n0 + Cfg::BNH * rank);
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % S;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                        raise_abort(abort_flag, p.status);
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cfg::STAGE_BYTES);
+                    const uint32_t bar = full_leader0 + 8 * s;
+                    const int32_t kc = (kb0 + kb) * Cfg::BK;
+                    const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_2d_pair(slot + g * Cfg::A_BOX_BYTES, &tmA, ma + 32 * g, kc, bar);
+                    uint32_t b_slot = slot + Cfg::A_BYTES;
+                    if (SPLIT3) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            tma_load_2d_pair(slot + Cfg::A_BYTES + g * Cfg::A_BOX_BYTES, &tmAs, ma + 32 * g, kc, bar);
+                        b_slot = slot + 2 * Cfg::A_BYTES;
+                        tma_load_2d_pair(b_slot + Cfg::B_BYTES, &tmBs, kc, nb, bar);
+                    }
+                    tma_load_2d_pair(b_slot, &tmB, kc, nb, bar);
+                }
+            }
+            if (leader) {
+                // Let every copy of the pair land before the CTAs may retire (CTA 0's
+                // full barriers count both CTAs' bytes).
+                for (int j = max(0, it - S); j < it; ++j)
+                    mbar_wait_bounded(full0 + 8 * (j % S), (j / S) & 1, p.timeout_ns, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (CTA 0 of the pair) ----------------
+        if (leader && lane == 0) {
+            int it = 0, lu = 0;
+            bool ok = true;
+            for (int u = pair; u < units && ok; u += pairs, ++lu) {
+                int64_t m0, n0;
+                int slice, kb0, nkb;
+                unit_geometry(u, m0, n0, slice, kb0, nkb);
+                const int buf = lu & 1;
+                if (!mbar_wait_bounded(acc_empty0 + 8 * buf, ((lu >> 1) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                    raise_abort(abort_flag, p.status);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem + buf * BN;
+                uint32_t accumulate = 0;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % S;
+                    if (!mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
+                        raise_abort(abort_flag, p.status);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+                    const uint32_t a_big = slot;
+                    const uint32_t a_small = slot + Cfg::A_BYTES;
+                    const uint32_t b_big = slot + Cfg::OPS * Cfg::A_BYTES;
+                    const uint32_t b_small = b_big + Cfg::B_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
+                        const uint64_t ad = smem_desc(a_big + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
+                        const uint64_t bd = smem_desc(b_big + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
+                        if (SPLIT3) {
+                            const uint64_t asd =
+                                smem_desc(a_small + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
+                            const uint64_t bsd = smem_desc(b_small + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
+                            mma_tf32_pair(d, asd, bd, Cfg::IDESC, accumulate);
+                            accumulate = 1;
+                            mma_tf32_pair(d, ad, bsd, Cfg::IDESC, 1);
+                            mma_tf32_pair(d, ad, bd, Cfg::IDESC, 1);
+                        } else {
+                            mma_tf32_pair(d, ad, bd, Cfg::IDESC, accumulate);
+                            accumulate = 1;
+                        }
+                    }
+                    mma_commit_pair(empty0 + 8 * s);  // both CTAs' slot s reusable after these MMAs
+                }
+                if (ok) mma_commit_pair(acc_full0 + 8 * buf);  // unit's accumulator complete
+            }
+            mma_commit_pair_local(mma_done);  // every MMA issued here has completed
+            mbar_wait_bounded(mma_done, 0, p.timeout_ns, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t acc_empty_leader0 = map_to_rank(acc_empty0, 0);
+        const float alpha = p.alpha, beta = p.beta;
+        int lu = 0;
+        for (int u = pair; u < units; u += pairs, ++lu) {
+            int64_t m0, n0;
+            int slice, kb0, nkb;
+            unit_geometry(u, m0, n0, slice, kb0, nkb);
+            const int buf = lu & 1;
+            const bool ready = __all_sync(
+                0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * buf, (lu >> 1) & 1, p.timeout_ns, abort_flag));
+            if (!ready) {
+                if (lane == 0) raise_abort(abort_flag, p.status);
+                break;
+            }
+            tc_fence_after_sync();
+            const int64_t i = m0 + Cfg::BM * rank + 32 * q + lane;
+            const bool row_ok = i < p.m;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int64_t jb = n0 + 32 * c;
+                if (jb >= p.n) break;  // uniform across the warp
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(lane_base + 32 * c, v);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
+                if (p.split > 1) {
+                    float* dst = p.P + slice * p.p_stride + jb * p.ldp + i;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (t < jn) dst[t * p.ldp] = __uint_as_float(v[t]);
+                } else {
+                    float* dst = p.C + jb * p.ldc + i;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        if (t < jn) {
+                            float o = alpha * __uint_as_float(v[t]);
+                            if (beta != 0.0f) o = fmaf(beta, dst[t * p.ldc], o);
+                            dst[t * p.ldc] = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acc_empty_leader0 + 8 * buf);  // buffer free for the next unit
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer may still read its shared memory or barriers
+    if (warp == 1) {
+        tc_fence_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Cfg::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int BN, bool SPLIT3>
+struct Launcher {
+    static cudaError_t run(const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b, const CUtensorMap& bs,
+                           const GemmParams& p, int units, int num_sms, cudaStream_t st, int* pairs_out) {
+        using Cfg = Tc2Cfg<BN, SPLIT3>;
+        auto kern = tc2_gemm_kernel<BN, SPLIT3>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(Cfg::SMEM));
+        if (e != cudaSuccess) return e;
+        // Pairs that can be resident at once (clusters must fit inside GPCs).
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM;
+        cfg.stream = st;
+        int max_clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+        if (e != cudaSuccess || max_clusters <= 0) {
+            cudaGetLastError();
+            max_clusters = num_sms / 2;
+        }
+        int pairs = units < max_clusters ? units : max_clusters;
+        if (pairs < 1) pairs = 1;
+        *pairs_out = pairs;
+        kern<<<dim3(2 * pairs), Cfg::THREADS, Cfg::SMEM, st>>>(a, as, b, bs, p);
+        return cudaGetLastError();
+    }
+};
+
+}  // namespace
+
+int tc2_stages(int bn, bool split3) {
+    if (split3) return bn == 128 ? Tc2Cfg<128, true>::STAGES : Tc2Cfg<256, true>::STAGES;
+    return bn == 128 ? Tc2Cfg<128, false>::STAGES : Tc2Cfg<256, false>::STAGES;
+}
+
+size_t tc2_smem_bytes(int bn, bool split3) {
+    if (split3) return bn == 128 ? Tc2Cfg<128, true>::SMEM : Tc2Cfg<256, true>::SMEM;
+    return bn == 128 ? Tc2Cfg<128, false>::SMEM : Tc2Cfg<256, false>::SMEM;
+}
+
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
+                       const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3, int units, int num_sms,
+                       cudaStream_t stream, int* pairs_launched) {
+    if (bn == 128)
+        return split3 ? Launcher<128, true>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched)
+                      : Launcher<128, false>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched);
+    if (bn == 256)
+        return split3 ? Launcher<256, true>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched)
+                      : Launcher<256, false>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pg

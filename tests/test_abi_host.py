@@ -110,9 +110,11 @@ def plan(m, n, k, mode="ffma", transa="N", transb="N", lda=None, ldb=None, ldc=N
 def test_plan_square_uses_wide_tiles_and_no_split(lib):
     for mode in ("ffma", "tf32", "3xtf32"):
         p = plan(8192, 8192, 8192, mode)
-        bn = 128 if mode == "ffma" else 256  # FFMA: 128 x 128 tiles, two CTAs per SM
-        assert p["bn"] == bn and p["split_k"] == 1 and p["tiles_m"] == 64 and p["tiles_n"] == 8192 // bn
-        assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc")
+        # FFMA: 128 x 128 tiles, two CTAs per SM; tensor cores: 256 x 256 tiles on SM pairs
+        bm, bn = (128, 128) if mode == "ffma" else (256, 256)
+        assert p["bn"] == bn and p["bm"] == bm and p["split_k"] == 1
+        assert p["tiles_m"] == 8192 // bm and p["tiles_n"] == 8192 // bn
+        assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc2")
         assert p["ctas_per_sm"] == (2 if mode == "ffma" else 1)
     assert plan(8192, 8192, 8192, "ffma")["prep_a_name"] == "none"
     assert plan(8192, 8192, 8192, "3xtf32")["prep_a_name"] == "split"
@@ -127,6 +129,15 @@ def test_plan_skinny_k_uses_deterministic_split(lib):
     assert p["launches"] == 2 and p["workspace_bytes"] >= p["split_k"] * 128 * 128 * 4
     tall = plan(8192, 64, 8192, "tf32")
     assert tall["bn"] == 64 and tall["tiles_m"] == 64 and tall["split_k"] == 2
+
+
+def test_plan_pair_kernel_only_above_128_rows(lib):
+    assert plan(128, 4096, 4096, "tf32")["kernel_name"] == "tc"       # one SM tile covers m
+    assert plan(129, 4096, 4096, "tf32")["kernel_name"] == "tc2"
+    assert plan(4096, 64, 4096, "3xtf32")["kernel_name"] == "tc"      # 64-wide tile: single SM
+    small = plan(512, 512, 65536, "tf32")                              # 2 x 2 pair tiles -> split K over 76 pairs
+    assert small["kernel_name"] == "tc2" and small["tiles_m"] * small["tiles_n"] == 4
+    assert small["split_k"] == 76 // 4
 
 
 def test_plan_misaligned_ld_copies_operand(lib):
