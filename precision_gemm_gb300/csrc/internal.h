@@ -28,6 +28,7 @@ struct GemmParams {
     int32_t group_m;         // rasterisation: tile rows per group
     int32_t c_vec;           // C 16-byte aligned and ldc % 4 == 0
     int32_t debug_flags;
+    int32_t a3d;             // tcgen05 kernels: A tensor map is 3-D {32, k, m/32} (one box per 128 rows)
     uint64_t timeout_ns;     // limit of every bounded wait
     int* status;             // per-device status word
 };
@@ -56,6 +57,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUt
 
 // tcgen05 kernel on SM pairs (cta_group::2, persistent, double-buffered TMEM):
 // pair tile 256 x bn, bn in {128, 256}; launches min(units, resident pairs) pairs.
+int tc2_bk(bool split3);
 int tc2_stages(int bn, bool split3);
 size_t tc2_smem_bytes(int bn, bool split3);
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,

@@ -33,6 +33,13 @@ __device__ int g_device_status;
 
 namespace {
 
+// Tile rows per rasterisation group (a compile-time tunable; 4, 8 and 16 measured
+// within noise of each other at 8192^3).
+#ifndef PG_GROUP_M
+#define PG_GROUP_M 16
+#endif
+
+
 constexpr int kMaxDevices = 64;
 constexpr const char* kVersion = "precision_gemm_gb300 0.1.0 (sm_103a; FFMA, TF32, 3xTF32)";
 
@@ -139,7 +146,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     const bool pair = tc && m > kBM && bn >= 128;
     pl->kernel = !tc ? SGEMM_KERNEL_FFMA : (pair ? SGEMM_KERNEL_TC2 : SGEMM_KERNEL_TC);
     pl->bm = pair ? 2 * kBM : kBM;
-    pl->bk = tc ? tc_bk(split3) : kFfmaBK;
+    pl->bk = !tc ? kFfmaBK : (pair ? tc2_bk(split3) : tc_bk(split3));
     pl->stages = !tc ? ffma_stages(bn) : (pair ? tc2_stages(bn, split3) : tc_stages(bn, split3));
     pl->threads = tc ? tc_threads() : ffma_threads(bn);
     pl->ctas_per_sm = tc ? 1 : ffma_ctas_per_sm(bn);
@@ -281,6 +288,28 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// M-major A (rows x cols, leading dimension ld, rows % 32 == 0) as the 3-D tensor
+// {32 rows, cols, rows / 32} with box {32, box_cols, 4}: one copy fetches 128 rows
+// as four [box_cols][32] row groups, the layout four 2-D boxes of 32 rows give.
+// Row groups past rows/32 are out of range of the third dimension and read as
+// zero, so no element beyond the matrix is touched.
+int encode_a3d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
+               CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows / 32)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, 32 * 4};
+    const cuuint32_t box[3] = {32, box_cols, 4};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled (3-D) failed (%d) for a %lld x %lld matrix, ld %lld",
+                    static_cast<int>(r), (long long)rows, (long long)cols, (long long)ld);
+    return 0;
+}
+
 // 2-D fp32 column-major matrix rows x cols with leading dimension ld (elements),
 // box {box_rows, box_cols}; out-of-range elements of a box read as zero.
 int encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
@@ -319,13 +348,18 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, const float* a_big, const f
         const bool pair = pl.kernel == SGEMM_KERNEL_TC2;
         const uint32_t b_cols = pair ? pl.bn / 2 : pl.bn;
         const CUtensorMapSwizzle bsw = pl.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B))) return rc;
+        const CUtensorMapSwizzle asw = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+        gp.a3d = (m % 32 == 0) ? 1 : 0;
+        auto encode_a = [&](CUtensorMap* map, const float* base) {
+            return gp.a3d ? encode_a3d(map, base, m, k, pl.ld_a, pl.bk, asw)
+                          : encode_2d(map, base, m, k, pl.ld_a, 32, pl.bk, asw);
+        };
+        if ((rc = encode_a(&tmA, a_big))) return rc;
         if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, pl.bk, b_cols, bsw))) return rc;
         tmAs = tmA;
         tmBs = tmB;
         if (split3) {
-            if ((rc = encode_2d(&tmAs, a_small, m, k, pl.ld_a, 32, pl.bk, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)))
-                return rc;
+            if ((rc = encode_a(&tmAs, a_small))) return rc;
             if ((rc = encode_2d(&tmBs, b_small, k, n, pl.ld_b, pl.bk, b_cols, bsw))) return rc;
         }
         if (pair) {
@@ -418,7 +452,7 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     gp.tiles_n = pl.tiles_n;
     gp.kb_total = pl.k_blocks;
     gp.kb_per_split = pl.k_blocks_per_split;
-    gp.group_m = 16;
+    gp.group_m = PG_GROUP_M;
     gp.c_vec = aligned16(C) && (ldc % 4 == 0);
     gp.debug_flags = g_debug.load();
     gp.timeout_ns = g_timeout_ns.load();
@@ -509,7 +543,7 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     gp.tiles_n = pl.tiles_n;
     gp.kb_total = pl.k_blocks;
     gp.kb_per_split = pl.k_blocks_per_split;
-    gp.group_m = 16;
+    gp.group_m = PG_GROUP_M;
     gp.c_vec = aligned16(C) && (ldc % 4 == 0);
     gp.debug_flags = g_debug.load();
     gp.timeout_ns = g_timeout_ns.load();

@@ -72,6 +72,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate) {
     asm volatile(
@@ -101,6 +110,11 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
 template <int BN, bool SPLIT3>
 struct Tc2Cfg {
     static constexpr int BM = kBM;               // rows per CTA (256 per pair)
+// Shared-memory budget of the operand ring (a compile-time tunable; one more slot
+// than the default measured no faster: the feed rate, not latency, bounds TF32).
+#ifndef PG_TC2_RING_BYTES
+#define PG_TC2_RING_BYTES (200 * 1024)
+#endif
     static constexpr int BK = SPLIT3 ? 16 : 32;
     static constexpr int OPS = SPLIT3 ? 2 : 1;
     static constexpr int BNH = BN / 2;           // B columns staged per CTA
@@ -108,8 +122,8 @@ struct Tc2Cfg {
     static constexpr int B_BYTES = BNH * BK * 4;
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
     static constexpr int STAGE_BYTES = OPS * (A_BYTES + B_BYTES);
-    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int STAGES_RAW = (PG_TC2_RING_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
     static constexpr int THREADS = 192;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
@@ -218,14 +232,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t bar = full_leader0 + 8 * s;
                     const int32_t kc = (kb0 + kb) * Cfg::BK;
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+                    // A: one 3-D box {32 rows, BK, 4 row groups} when m % 32 == 0, else four
+                    // 2-D boxes of 32 rows (both land as 4 x [BK][32] row groups).
+                    auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
+                        if (p.a3d) {
+                            tma_load_3d_pair(dst, map, 0, kc, ma / 32, bar);
+                        } else {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
-                        tma_load_2d_pair(slot + g * Cfg::A_BOX_BYTES, &tmA, ma + 32 * g, kc, bar);
+                            for (int g = 0; g < 4; ++g)
+                                tma_load_2d_pair(dst + g * Cfg::A_BOX_BYTES, map, ma + 32 * g, kc, bar);
+                        }
+                    };
+                    load_a(slot, &tmA);
                     uint32_t b_slot = slot + Cfg::A_BYTES;
                     if (SPLIT3) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            tma_load_2d_pair(slot + Cfg::A_BYTES + g * Cfg::A_BOX_BYTES, &tmAs, ma + 32 * g, kc, bar);
+                        load_a(slot + Cfg::A_BYTES, &tmAs);
                         b_slot = slot + 2 * Cfg::A_BYTES;
                         tma_load_2d_pair(b_slot + Cfg::B_BYTES, &tmBs, kc, nb, bar);
                     }
@@ -387,6 +408,8 @@ struct Launcher {
 };
 
 }  // namespace
+
+int tc2_bk(bool split3) { return split3 ? Tc2Cfg<256, true>::BK : Tc2Cfg<256, false>::BK; }
 
 int tc2_stages(int bn, bool split3) {
     if (split3) return bn == 128 ? Tc2Cfg<128, true>::STAGES : Tc2Cfg<256, true>::STAGES;

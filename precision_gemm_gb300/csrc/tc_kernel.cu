@@ -136,16 +136,22 @@ __global__ void __launch_bounds__(192, 1)
                     mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
                     const int32_t kc = (kb0 + it) * Cfg::BK;
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+                    // A: one 3-D box {32 rows, BK, 4 row groups} when m % 32 == 0, else four
+                    // 2-D boxes of 32 rows (both land as 4 x [BK][32] row groups).
+                    auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
+                        if (p.a3d) {
+                            tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(m0 / 32), full);
+                        } else {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
-                        tma_load_2d(slot + g * Cfg::A_BOX_BYTES, &tmA, static_cast<int32_t>(m0 + 32 * g), kc,
-                                    full);
+                            for (int g = 0; g < 4; ++g)
+                                tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(m0 + 32 * g), kc,
+                                            full);
+                        }
+                    };
+                    load_a(slot, &tmA);
                     uint32_t b_slot = slot + Cfg::A_BYTES;
                     if (SPLIT3) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            tma_load_2d(slot + Cfg::A_BYTES + g * Cfg::A_BOX_BYTES, &tmAs,
-                                        static_cast<int32_t>(m0 + 32 * g), kc, full);
+                        load_a(slot + Cfg::A_BYTES, &tmAs);
                         b_slot = slot + 2 * Cfg::A_BYTES;
                         tma_load_2d(b_slot + Cfg::B_BYTES, &tmBs, kc, static_cast<int32_t>(n0), full);
                     }
