@@ -140,7 +140,8 @@ def test_transposed_operands(mode, trans):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
-                                 (128, 256, 32), (257, 513, 1031), (64, 64, 200000)])
+                                 (128, 256, 32), (257, 513, 1031), (64, 64, 200000), (160, 200, 300), (288, 130, 77),
+                                 (416, 1000, 2048)])
 def test_ragged_and_small(mode, mnk):
     m, n, k = mnk
     p = synth.Problem(m, n, k, lda=m + 1, ldb=k + 2, ldc=m + 3, alpha=1.25, beta=-0.75, dist="normal", seed=11)
