@@ -20,6 +20,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/precision_gemm.h"
 #include "internal.h"
@@ -552,6 +553,44 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     return launch_gemm(pl, false, A, A, B, B, m, n, k, gp, ds->sms, st);
 }
 
+// ---- the host-array entry: internal copy streams ------------------------------------------
+
+// Two non-blocking streams per device for sgemm_host's copies in and out, with a
+// pool of events that order them against the caller's stream.  One mutex per
+// device serialises sgemm_host calls that use them (each call is synchronous).
+struct HostPipe {
+    std::mutex mu;
+    cudaStream_t in = nullptr, out = nullptr;
+    std::vector<cudaEvent_t> events;
+    cudaEvent_t ev(size_t i) {
+        while (events.size() <= i) {
+            cudaEvent_t e = nullptr;
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+            events.push_back(e);
+        }
+        return events[i];
+    }
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_init_mu;
+
+int host_pipe(int dev, HostPipe** out) {
+    std::lock_guard<std::mutex> lk(g_pipe_init_mu);
+    HostPipe& hp = g_pipe[dev];
+    cudaError_t e;
+    if (!hp.in && (e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess)
+        return fail_cuda(e, "cudaStreamCreateWithFlags");
+    if (!hp.out && (e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess)
+        return fail_cuda(e, "cudaStreamCreateWithFlags");
+    {
+        std::lock_guard<std::mutex> lk2(hp.mu);
+        for (size_t i = 0; i < 18; ++i)
+            if (!hp.ev(i)) return fail(SGEMM_ERR_CUDA, "cudaEventCreateWithFlags failed");
+    }
+    *out = &hp;
+    return 0;
+}
+
 }  // namespace
 }  // namespace pg
 
@@ -589,24 +628,75 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
     float* dA = reinterpret_cast<float*>(static_cast<char*>(stage));
     float* dB = reinterpret_cast<float*>(static_cast<char*>(stage) + a_bytes);
     float* dC = reinterpret_cast<float*>(static_cast<char*>(stage) + a_bytes + b_bytes);
-    cudaError_t e;
-    if (reads_ab) {
-        if ((e = cudaMemcpy2DAsync(dA, lda_d * 4, A, lda * 4, ra * 4, ca, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return fail_cuda(e, "copy of A to the device");
-        if ((e = cudaMemcpy2DAsync(dB, ldb_d * 4, B, ldb * 4, rb * 4, cb, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return fail_cuda(e, "copy of B to the device");
+
+    // Column slabs of C: A is copied in once; each slab's columns of B (and of C
+    // when beta != 0) are copied in on one internal stream, the slab is computed
+    // on `stream`, and its result is copied out on a second internal stream, so
+    // the copies of one slab overlap the arithmetic of its neighbours.  Slabs
+    // stay at least 2048 columns wide so each product still fills the GPU.
+    const int slabs = (reads_ab && is_notrans(transb) && n >= 4096) ? static_cast<int>(std::min<int64_t>(8, n / 2048))
+                                                                      : 1;
+    HostPipe* hp = nullptr;
+    if (slabs > 1 && (rc = host_pipe(dev, &hp))) return rc;
+    std::unique_lock<std::mutex> lk;
+    if (hp) lk = std::unique_lock<std::mutex>(hp->mu);
+    cudaStream_t s_in = hp ? hp->in : st;
+    cudaStream_t s_out = hp ? hp->out : st;
+    cudaError_t e = cudaSuccess;
+    auto note = [&](cudaError_t err, const char* what) {
+        if (err != cudaSuccess && rc == 0) rc = fail_cuda(err, what);
+        return rc == 0;
+    };
+    if (hp) {  // the internal streams start after the work already queued on `stream`
+        note(cudaEventRecord(hp->ev(0), st), "cudaEventRecord");
+        note(cudaStreamWaitEvent(s_in, hp->ev(0), 0), "cudaStreamWaitEvent");
+        note(cudaStreamWaitEvent(s_out, hp->ev(0), 0), "cudaStreamWaitEvent");
     }
-    if (beta != 0.0f) {
-        if ((e = cudaMemcpy2DAsync(dC, ldc_d * 4, C, ldc * 4, m * 4, n, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return fail_cuda(e, "copy of C to the device");
+    if (rc == 0 && reads_ab) {
+        note(cudaMemcpy2DAsync(dA, lda_d * 4, A, lda * 4, ra * 4, ca, cudaMemcpyHostToDevice, s_in),
+             "copy of A to the device");
+        if (hp) {
+            note(cudaEventRecord(hp->ev(1), s_in), "cudaEventRecord");
+            note(cudaStreamWaitEvent(st, hp->ev(1), 0), "cudaStreamWaitEvent");
+        }
     }
-    rc = run(transa, transb, m, n, k, alpha, reads_ab ? dA : nullptr, reads_ab ? lda_d : 1, reads_ab ? dB : nullptr,
-             reads_ab ? ldb_d : 1, beta, dC, ldc_d, mode, st);
-    if (rc) return rc;
-    if ((e = cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_d * 4, m * 4, n, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return fail_cuda(e, "copy of C to the host");
-    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-    return 0;
+    for (int sl = 0; sl < slabs && rc == 0; ++sl) {
+        const int64_t j0 = n * sl / slabs, j1 = n * (sl + 1) / slabs, w = j1 - j0;
+        if (reads_ab) {
+            // slabs > 1 only with B untransposed: columns j0..j1 of B are contiguous storage columns
+            const int64_t b_cols = (slabs > 1) ? w : cb;
+            note(cudaMemcpy2DAsync(dB + j0 * ldb_d, ldb_d * 4, B + j0 * ldb, ldb * 4, rb * 4, b_cols,
+                                   cudaMemcpyHostToDevice, s_in),
+                 "copy of B to the device");
+        }
+        if (rc == 0 && beta != 0.0f)
+            note(cudaMemcpy2DAsync(dC + j0 * ldc_d, ldc_d * 4, C + j0 * ldc, ldc * 4, m * 4, w, cudaMemcpyHostToDevice,
+                                   s_in),
+                 "copy of C to the device");
+        if (rc == 0 && hp) {
+            note(cudaEventRecord(hp->ev(2 + 2 * sl), s_in), "cudaEventRecord");
+            note(cudaStreamWaitEvent(st, hp->ev(2 + 2 * sl), 0), "cudaStreamWaitEvent");
+        }
+        if (rc == 0)
+            rc = run(transa, transb, m, w, k, alpha, reads_ab ? dA : nullptr, reads_ab ? lda_d : 1,
+                     reads_ab ? dB + j0 * ldb_d : nullptr, reads_ab ? ldb_d : 1, beta, dC + j0 * ldc_d, ldc_d, mode, st);
+        if (rc == 0 && hp) {
+            note(cudaEventRecord(hp->ev(3 + 2 * sl), st), "cudaEventRecord");
+            note(cudaStreamWaitEvent(s_out, hp->ev(3 + 2 * sl), 0), "cudaStreamWaitEvent");
+        }
+        if (rc == 0)
+            note(cudaMemcpy2DAsync(C + j0 * ldc, ldc * 4, dC + j0 * ldc_d, ldc_d * 4, m * 4, w, cudaMemcpyDeviceToHost,
+                                   s_out),
+                 "copy of C to the host");
+    }
+    // Every queued copy touches the caller's host arrays: wait for all of them
+    // (also after a failure) before returning.
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess && rc == 0) rc = fail_cuda(e, "cudaStreamSynchronize");
+    if (hp) {
+        if ((e = cudaStreamSynchronize(s_in)) != cudaSuccess && rc == 0) rc = fail_cuda(e, "cudaStreamSynchronize");
+        if ((e = cudaStreamSynchronize(s_out)) != cudaSuccess && rc == 0) rc = fail_cuda(e, "cudaStreamSynchronize");
+    }
+    return rc;
 }
 
 PG_EXPORT int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,

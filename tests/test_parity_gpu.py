@@ -206,6 +206,26 @@ def test_host_buffers_match_device_path(mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_host_buffers_pipelined_slabs(mode):
+    """n >= 4096: sgemm_host overlaps the copies of column slabs with the arithmetic
+    of their neighbours (internal copy streams); the result must still match the
+    oracle, and the ld gap of the host C must stay untouched."""
+    p = synth.Problem(1000, 4100, 300, lda=1003, ldb=301, ldc=1005, alpha=1.25, beta=0.5, dist="normal", seed=29)
+    A, B, C = synth.make(p)
+    Ch = C.clone().pin_memory()
+    pg.sgemm_host("N", "N", p.m, p.n, p.k, p.alpha, A.pin_memory(), p.lda, B.pin_memory(), p.ldb, p.beta, Ch,
+                  p.ldc, mode)
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, Ch), cref, den, oracle.TOL[mode])
+    assert res["ok"], res
+    assert H.padding_intact(p, Ch, C)
+    # pageable host memory takes the same path
+    Cp = C.clone()
+    pg.sgemm_host("N", "N", p.m, p.n, p.k, p.alpha, A, p.lda, B, p.ldb, p.beta, Cp, p.ldc, mode)
+    assert oracle.check(H.logical(p, Cp), cref, den, oracle.TOL[mode])["ok"]
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_launch_counter_counts_kernels(mode):
     for p in (synth.Problem(256, 256, 256), synth.Problem(4096, 4096, 512)):
         A, B, C = synth.make(p)
