@@ -29,6 +29,9 @@ struct GemmParams {
     int32_t c_vec;           // C 16-byte aligned and ldc % 4 == 0
     int32_t debug_flags;
     int32_t a3d;             // tcgen05 kernels: A tensor map is 3-D {32, k, m/32} (one box per 128 rows)
+    int32_t a_kmajor;        // tcgen05 kernels: A is read K-major (transa = 'T'), else M-major
+    int32_t b_mnmajor;       // tcgen05 kernels: B is read N-major (transb = 'T'), else K-major
+    int32_t b3d;             // tcgen05 kernels, N-major B: tensor map 3-D {32, k, n/32}
     uint64_t timeout_ns;     // limit of every bounded wait
     int* status;             // per-device status word
 };

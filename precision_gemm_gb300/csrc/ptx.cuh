@@ -204,6 +204,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     return d;
 }
 
+// Descriptor of the 8-deep k-step kk of an operand tile at shared address `tile`
+// (BK k-values per ring slot), in one of the two canonical TF32 layouts:
+//   K-major  : one row of BK floats per M/N index, the 128-byte swizzle (BK 32,
+//              8-row atoms of 1 KiB) or 64-byte swizzle (BK 16, 512-B atoms);
+//              the k-step starts 32 bytes further into each row.
+//   M/N-major: groups of 32 M/N indices, each BK rows of 128 bytes (one per k) in
+//              the 128-byte swizzle with 32-byte atoms; leading byte offset (between
+//              groups) 128*BK, stride byte offset (between 4-row atoms) 512; the
+//              k-step starts 8 rows (1 KiB) further.
+template <int BK>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int kk, bool k_major) {
+    if (k_major)
+        return smem_desc(tile + 32 * kk, 16, BK == 32 ? 1024 : 512, BK == 32 ? kSwizzle128B : kSwizzle64B);
+    return smem_desc(tile + 1024 * kk, 128 * BK, 512, kSwizzle128B32);
+}
+
 // Instruction descriptor for kind::tf32 with FP32 accumulation: D format F32
 // (bits 4-5 = 1), A and B format TF32 (bits 7-9 and 10-12 = 2), A major-ness
 // (bit 15: 1 = M-major), B major-ness (bit 16: 0 = K-major), N/8 in bits 17-22,

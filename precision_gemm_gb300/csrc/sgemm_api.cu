@@ -122,19 +122,29 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     const bool split3 = mode == SGEMM_3XTF32;
 
     // Operand preparation: TMA needs a 16-byte aligned base and a leading
-    // dimension that is a multiple of 16 bytes; the kernels read A M-major and
-    // B K-major, i.e. both not transposed.
-    const bool a_inplace = is_notrans(transa) && aligned16(A) && (lda % 4 == 0);
-    const bool b_inplace = is_notrans(transb) && aligned16(B) && (ldb % 4 == 0);
+    // dimension that is a multiple of 16 bytes.  The tensor-core kernels read
+    // either orientation of A and B (K-major or M/N-major descriptors), so their
+    // copies and 3xTF32 splits keep the stored orientation; the FFMA kernel reads
+    // A M-major and B K-major only, so a transposed operand is copied transposed.
+    const bool a_ok = aligned16(A) && (lda % 4 == 0);
+    const bool b_ok = aligned16(B) && (ldb % 4 == 0);
     if (split3) {
         pl->prep_a = SGEMM_PREP_SPLIT;
         pl->prep_b = SGEMM_PREP_SPLIT;
+    } else if (tc) {
+        pl->prep_a = a_ok ? SGEMM_PREP_NONE : SGEMM_PREP_COPY;
+        pl->prep_b = b_ok ? SGEMM_PREP_NONE : SGEMM_PREP_COPY;
     } else {
-        pl->prep_a = a_inplace ? SGEMM_PREP_NONE : (is_notrans(transa) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
-        pl->prep_b = b_inplace ? SGEMM_PREP_NONE : (is_notrans(transb) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
+        pl->prep_a = (a_ok && is_notrans(transa)) ? SGEMM_PREP_NONE
+                                                  : (is_notrans(transa) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
+        pl->prep_b = (b_ok && is_notrans(transb)) ? SGEMM_PREP_NONE
+                                                  : (is_notrans(transb) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
     }
-    pl->ld_a = pl->prep_a == SGEMM_PREP_NONE ? lda : round_up(m, 4);
-    pl->ld_b = pl->prep_b == SGEMM_PREP_NONE ? ldb : round_up(k, 4);
+    // Stored rows of each operand as the kernel reads it.
+    const int64_t rows_a = (tc && !is_notrans(transa)) ? k : m;
+    const int64_t rows_b = (tc && !is_notrans(transb)) ? n : k;
+    pl->ld_a = pl->prep_a == SGEMM_PREP_NONE ? lda : round_up(rows_a, 4);
+    pl->ld_b = pl->prep_b == SGEMM_PREP_NONE ? ldb : round_up(rows_b, 4);
 
     // Tile width: 64 for n <= 64; otherwise 128 for the FFMA kernel (two CTAs per
     // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05.
@@ -177,8 +187,8 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
 
     size_t ws = 0;
     const int parts = split3 ? 2 : 1;
-    if (pl->prep_a != SGEMM_PREP_NONE) ws += parts * region(pl->ld_a * k);
-    if (pl->prep_b != SGEMM_PREP_NONE) ws += parts * region(pl->ld_b * n);
+    if (pl->prep_a != SGEMM_PREP_NONE) ws += parts * region(pl->ld_a * (rows_a == m ? k : m));
+    if (pl->prep_b != SGEMM_PREP_NONE) ws += parts * region(pl->ld_b * (rows_b == k ? n : k));
     if (split > 1) ws += region(split * round_up(m, 4) * n);
     pl->workspace_bytes = ws;
     pl->launches = (pl->prep_a != SGEMM_PREP_NONE) + (pl->prep_b != SGEMM_PREP_NONE) + 1 + (split > 1);
@@ -289,18 +299,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// M-major A (rows x cols, leading dimension ld, rows % 32 == 0) as the 3-D tensor
-// {32 rows, cols, rows / 32} with box {32, box_cols, 4}: one copy fetches 128 rows
-// as four [box_cols][32] row groups, the layout four 2-D boxes of 32 rows give.
-// Row groups past rows/32 are out of range of the third dimension and read as
-// zero, so no element beyond the matrix is touched.
-int encode_a3d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
-               CUtensorMapSwizzle swizzle) {
+// An M/N-major operand (rows x cols, leading dimension ld, rows % 32 == 0) as the
+// 3-D tensor {32 rows, cols, rows / 32} with box {32, box_cols, groups}: one copy
+// fetches 32 * groups rows as `groups` [box_cols][32] row groups, the layout that
+// `groups` 2-D boxes of 32 rows give.  Row groups past rows/32 are out of range of
+// the third dimension and read as zero, so no element beyond the matrix is read.
+int encode_mn3d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
+                uint32_t groups, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled is unavailable from the driver");
     const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows / 32)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, 32 * 4};
-    const cuuint32_t box[3] = {32, box_cols, 4};
+    const cuuint32_t box[3] = {32, box_cols, groups};
     const cuuint32_t elem[3] = {1, 1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
                           elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -333,8 +343,9 @@ int encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, i
 // Encode the tensor maps the planned kernel reads, launch it, then the split-K
 // reduction when the plan splits K.  Operands are in the kernels' layout here
 // (A M-major with ld pl.ld_a, B K-major with ld pl.ld_b).
-int launch_gemm(const sgemm_plan_t& pl, bool split3, const float* a_big, const float* a_small, const float* b_big,
-                const float* b_small, int64_t m, int64_t n, int64_t k, GemmParams& gp, int num_sms, cudaStream_t st) {
+int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmajor, const float* a_big,
+                const float* a_small, const float* b_big, const float* b_small, int64_t m, int64_t n, int64_t k,
+                GemmParams& gp, int num_sms, cudaStream_t st) {
     int rc;
     cudaError_t e;
     CUtensorMap tmA, tmB, tmAs, tmBs;
@@ -348,20 +359,32 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, const float* a_big, const f
         // pl.bk x (bn, or bn/2 per CTA on SM pairs).
         const bool pair = pl.kernel == SGEMM_KERNEL_TC2;
         const uint32_t b_cols = pair ? pl.bn / 2 : pl.bn;
-        const CUtensorMapSwizzle bsw = pl.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        const CUtensorMapSwizzle asw = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
-        gp.a3d = (m % 32 == 0) ? 1 : 0;
+        // K-major operands: rows of BK floats, 128- or 64-byte swizzle.  M/N-major
+        // operands: groups of 32 rows in the 32-byte-atom 128-byte swizzle, as one
+        // 3-D box when the extent is a multiple of 32, else as 2-D boxes.
+        const CUtensorMapSwizzle ksw = pl.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        const CUtensorMapSwizzle msw = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+        gp.a_kmajor = a_kmajor ? 1 : 0;
+        gp.b_mnmajor = b_mnmajor ? 1 : 0;
+        gp.a3d = (!a_kmajor && m % 32 == 0) ? 1 : 0;
+        gp.b3d = (b_mnmajor && n % 32 == 0) ? 1 : 0;
         auto encode_a = [&](CUtensorMap* map, const float* base) {
-            return gp.a3d ? encode_a3d(map, base, m, k, pl.ld_a, pl.bk, asw)
-                          : encode_2d(map, base, m, k, pl.ld_a, 32, pl.bk, asw);
+            if (a_kmajor) return encode_2d(map, base, k, m, pl.ld_a, pl.bk, kBM, ksw);
+            return gp.a3d ? encode_mn3d(map, base, m, k, pl.ld_a, pl.bk, 4, msw)
+                          : encode_2d(map, base, m, k, pl.ld_a, 32, pl.bk, msw);
+        };
+        auto encode_b = [&](CUtensorMap* map, const float* base) {
+            if (!b_mnmajor) return encode_2d(map, base, k, n, pl.ld_b, pl.bk, b_cols, ksw);
+            return gp.b3d ? encode_mn3d(map, base, n, k, pl.ld_b, pl.bk, b_cols / 32, msw)
+                          : encode_2d(map, base, n, k, pl.ld_b, 32, pl.bk, msw);
         };
         if ((rc = encode_a(&tmA, a_big))) return rc;
-        if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, pl.bk, b_cols, bsw))) return rc;
+        if ((rc = encode_b(&tmB, b_big))) return rc;
         tmAs = tmA;
         tmBs = tmB;
         if (split3) {
             if ((rc = encode_a(&tmAs, a_small))) return rc;
-            if ((rc = encode_2d(&tmBs, b_small, k, n, pl.ld_b, pl.bk, b_cols, bsw))) return rc;
+            if ((rc = encode_b(&tmBs, b_small))) return rc;
         }
         if (pair) {
             int pairs = 0;
@@ -408,13 +431,16 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     const float* a_small = nullptr;
     if (pl.prep_a != SGEMM_PREP_NONE) {
         float* d = reinterpret_cast<float*>(cursor);
-        cursor += region(pl.ld_a * k);
+        const int64_t cols_a = (pl.kernel != SGEMM_KERNEL_FFMA && !is_notrans(transa)) ? m : k;
+        cursor += region(pl.ld_a * cols_a);
         float* ds2 = nullptr;
         if (parts == 2) {
             ds2 = reinterpret_cast<float*>(cursor);
-            cursor += region(pl.ld_a * k);
+            cursor += region(pl.ld_a * cols_a);
         }
-        if ((e = launch_prep(A, lda, !is_notrans(transa), m, k, d, ds2, pl.ld_a, ds->sms, st)) != cudaSuccess)
+        const bool tr = pl.prep_a == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into M-major
+        const bool kmaj = !tr && !is_notrans(transa);      // tensor cores: stored k x m, kept as is
+        if ((e = launch_prep(A, lda, tr, kmaj ? k : m, kmaj ? m : k, d, ds2, pl.ld_a, ds->sms, st)) != cudaSuccess)
             return fail_cuda(e, "operand preparation (A)");
         a_big = d;
         a_small = ds2;
@@ -423,13 +449,16 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     const float* b_small = nullptr;
     if (pl.prep_b != SGEMM_PREP_NONE) {
         float* d = reinterpret_cast<float*>(cursor);
-        cursor += region(pl.ld_b * n);
+        const int64_t cols_b = (pl.kernel != SGEMM_KERNEL_FFMA && !is_notrans(transb)) ? k : n;
+        cursor += region(pl.ld_b * cols_b);
         float* ds2 = nullptr;
         if (parts == 2) {
             ds2 = reinterpret_cast<float*>(cursor);
-            cursor += region(pl.ld_b * n);
+            cursor += region(pl.ld_b * cols_b);
         }
-        if ((e = launch_prep(B, ldb, !is_notrans(transb), k, n, d, ds2, pl.ld_b, ds->sms, st)) != cudaSuccess)
+        const bool tr = pl.prep_b == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into K-major
+        const bool nmaj = !tr && !is_notrans(transb);      // tensor cores: stored n x k, kept as is
+        if ((e = launch_prep(B, ldb, tr, nmaj ? n : k, nmaj ? k : n, d, ds2, pl.ld_b, ds->sms, st)) != cudaSuccess)
             return fail_cuda(e, "operand preparation (B)");
         b_big = d;
         b_small = ds2;
@@ -459,7 +488,9 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     gp.timeout_ns = g_timeout_ns.load();
     gp.status = ds->status;
 
-    return launch_gemm(pl, split3, a_big, a_small, b_big, b_small, m, n, k, gp, ds->sms, st);
+    const bool tcm = pl.kernel != SGEMM_KERNEL_FFMA;
+    return launch_gemm(pl, split3, tcm && !is_notrans(transa), tcm && !is_notrans(transb), a_big, a_small, b_big,
+                       b_small, m, n, k, gp, ds->sms, st);
 }
 
 // ---- the allocation-free variant (sgemm_noalloc) ---------------------------------------
@@ -550,7 +581,7 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     gp.timeout_ns = g_timeout_ns.load();
     gp.status = ds->status;
 
-    return launch_gemm(pl, false, A, A, B, B, m, n, k, gp, ds->sms, st);
+    return launch_gemm(pl, false, false, false, A, A, B, B, m, n, k, gp, ds->sms, st);
 }
 
 // ---- the host-array entry: internal copy streams ------------------------------------------

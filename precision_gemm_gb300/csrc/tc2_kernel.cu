@@ -127,11 +127,6 @@ struct Tc2Cfg {
     static constexpr int THREADS = 192;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
-    static constexpr uint32_t IDESC = idesc_tf32(2 * BM, BN, /*a_mn_major=*/true, /*b_mn_major=*/false);
-    static constexpr uint32_t A_LBO = 128 * BK;
-    static constexpr uint32_t A_SBO = 512;
-    static constexpr uint32_t B_SBO = (BK == 32) ? 1024 : 512;
-    static constexpr uint32_t B_LAYOUT = (BK == 32) ? kSwizzle128B : kSwizzle64B;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulator buffers
     static_assert(BN == 128 || BN == 256, "BN");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
@@ -234,8 +229,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
                     // A: one 3-D box {32 rows, BK, 4 row groups} when m % 32 == 0, else four
                     // 2-D boxes of 32 rows (both land as 4 x [BK][32] row groups).
+                    // A K-major (transa 'T'): one box of 128 rows x BK; A M-major: one 3-D box
+                    // or four 2-D boxes of 32 rows.  B K-major: one box of BN/2 columns;
+                    // B N-major (transb 'T'): BN/64 groups of 32 columns.
                     auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
-                        if (p.a3d) {
+                        if (p.a_kmajor) {
+                            tma_load_2d_pair(dst, map, kc, ma, bar);
+                        } else if (p.a3d) {
                             tma_load_3d_pair(dst, map, 0, kc, ma / 32, bar);
                         } else {
 #pragma unroll
@@ -243,14 +243,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                                 tma_load_2d_pair(dst + g * Cfg::A_BOX_BYTES, map, ma + 32 * g, kc, bar);
                         }
                     };
+                    auto load_b = [&](uint32_t dst, const CUtensorMap* map) {
+                        if (!p.b_mnmajor) {
+                            tma_load_2d_pair(dst, map, kc, nb, bar);
+                        } else if (p.b3d) {
+                            tma_load_3d_pair(dst, map, 0, kc, nb / 32, bar);
+                        } else {
+#pragma unroll
+                            for (int g = 0; g < Cfg::BNH / 32; ++g)
+                                tma_load_2d_pair(dst + g * Cfg::A_BOX_BYTES, map, nb + 32 * g, kc, bar);
+                        }
+                    };
                     load_a(slot, &tmA);
                     uint32_t b_slot = slot + Cfg::A_BYTES;
                     if (SPLIT3) {
                         load_a(slot + Cfg::A_BYTES, &tmAs);
                         b_slot = slot + 2 * Cfg::A_BYTES;
-                        tma_load_2d_pair(b_slot + Cfg::B_BYTES, &tmBs, kc, nb, bar);
+                        load_b(b_slot + Cfg::B_BYTES, &tmBs);
                     }
-                    tma_load_2d_pair(b_slot, &tmB, kc, nb, bar);
+                    load_b(b_slot, &tmB);
                 }
             }
             if (leader) {
@@ -265,6 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (leader && lane == 0) {
             int it = 0, lu = 0;
             bool ok = true;
+            const uint32_t idesc = idesc_tf32(2 * Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
             for (int u = pair; u < units && ok; u += pairs, ++lu) {
                 int64_t m0, n0;
                 int slice, kb0, nkb;
@@ -292,18 +304,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t b_small = b_big + Cfg::B_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-                        const uint64_t ad = smem_desc(a_big + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
-                        const uint64_t bd = smem_desc(b_big + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
+                        const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
+                        const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
                         if (SPLIT3) {
-                            const uint64_t asd =
-                                smem_desc(a_small + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
-                            const uint64_t bsd = smem_desc(b_small + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
-                            mma_tf32_pair(d, asd, bd, Cfg::IDESC, accumulate);
+                            const uint64_t asd = operand_desc<Cfg::BK>(a_small, kk, p.a_kmajor != 0);
+                            const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
+                            mma_tf32_pair(d, asd, bd, idesc, accumulate);
                             accumulate = 1;
-                            mma_tf32_pair(d, ad, bsd, Cfg::IDESC, 1);
-                            mma_tf32_pair(d, ad, bd, Cfg::IDESC, 1);
+                            mma_tf32_pair(d, ad, bsd, idesc, 1);
+                            mma_tf32_pair(d, ad, bd, idesc, 1);
                         } else {
-                            mma_tf32_pair(d, ad, bd, Cfg::IDESC, accumulate);
+                            mma_tf32_pair(d, ad, bd, idesc, accumulate);
                             accumulate = 1;
                         }
                     }

@@ -59,11 +59,6 @@ struct TcCfg {
     static constexpr int THREADS = 192;
     static constexpr int BAR_BYTES = (2 * STAGES + 1) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
-    static constexpr uint32_t IDESC = idesc_tf32(BM, BN, /*a_mn_major=*/true, /*b_mn_major=*/false);
-    static constexpr uint32_t A_LBO = 128 * BK;
-    static constexpr uint32_t A_SBO = 512;
-    static constexpr uint32_t B_SBO = (BK == 32) ? 1024 : 512;
-    static constexpr uint32_t B_LAYOUT = (BK == 32) ? kSwizzle128B : kSwizzle64B;
     static constexpr uint32_t TMEM_COLS = BN;  // power of two >= 32
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
@@ -138,8 +133,13 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
                     // A: one 3-D box {32 rows, BK, 4 row groups} when m % 32 == 0, else four
                     // 2-D boxes of 32 rows (both land as 4 x [BK][32] row groups).
+                    // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
+                    // box {32 rows, BK, 4 row groups} when m % 32 == 0, else four 2-D boxes
+                    // of 32 rows (both land as 4 x [BK][32] row groups).
                     auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
-                        if (p.a3d) {
+                        if (p.a_kmajor) {
+                            tma_load_2d(dst, map, kc, static_cast<int32_t>(m0), full);
+                        } else if (p.a3d) {
                             tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(m0 / 32), full);
                         } else {
 #pragma unroll
@@ -148,14 +148,28 @@ __global__ void __launch_bounds__(192, 1)
                                             full);
                         }
                     };
+                    // B K-major: one box of BN columns x BK.  B N-major (transb 'T'): BN/32
+                    // groups of 32 columns, as one 3-D box or as 2-D boxes.
+                    auto load_b = [&](uint32_t dst, const CUtensorMap* map) {
+                        if (!p.b_mnmajor) {
+                            tma_load_2d(dst, map, kc, static_cast<int32_t>(n0), full);
+                        } else if (p.b3d) {
+                            tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(n0 / 32), full);
+                        } else {
+#pragma unroll
+                            for (int g = 0; g < BN / 32; ++g)
+                                tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(n0 + 32 * g), kc,
+                                            full);
+                        }
+                    };
                     load_a(slot, &tmA);
                     uint32_t b_slot = slot + Cfg::A_BYTES;
                     if (SPLIT3) {
                         load_a(slot + Cfg::A_BYTES, &tmAs);
                         b_slot = slot + 2 * Cfg::A_BYTES;
-                        tma_load_2d(b_slot + Cfg::B_BYTES, &tmBs, kc, static_cast<int32_t>(n0), full);
+                        load_b(b_slot + Cfg::B_BYTES, &tmBs);
                     }
-                    tma_load_2d(b_slot, &tmB, kc, static_cast<int32_t>(n0), full);
+                    load_b(b_slot, &tmB);
                     issued = it + 1;
                 }
             }
@@ -167,6 +181,7 @@ __global__ void __launch_bounds__(192, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             uint32_t accumulate = 0;
+            const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
                 if (!mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
@@ -181,18 +196,17 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t b_small = b_big + Cfg::B_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-                    const uint64_t ad = smem_desc(a_big + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
-                    const uint64_t bd = smem_desc(b_big + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
+                    const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
+                    const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
                     if (SPLIT3) {
-                        const uint64_t asd =
-                            smem_desc(a_small + 1024 * kk, Cfg::A_LBO, Cfg::A_SBO, kSwizzle128B32);
-                        const uint64_t bsd = smem_desc(b_small + 32 * kk, 16, Cfg::B_SBO, Cfg::B_LAYOUT);
-                        mma_tf32(tmem, asd, bd, Cfg::IDESC, accumulate);
+                        const uint64_t asd = operand_desc<Cfg::BK>(a_small, kk, p.a_kmajor != 0);
+                        const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
+                        mma_tf32(tmem, asd, bd, idesc, accumulate);
                         accumulate = 1;
-                        mma_tf32(tmem, ad, bsd, Cfg::IDESC, 1);
-                        mma_tf32(tmem, ad, bd, Cfg::IDESC, 1);
+                        mma_tf32(tmem, ad, bsd, idesc, 1);
+                        mma_tf32(tmem, ad, bd, idesc, 1);
                     } else {
-                        mma_tf32(tmem, ad, bd, Cfg::IDESC, accumulate);
+                        mma_tf32(tmem, ad, bd, idesc, accumulate);
                         accumulate = 1;
                     }
                 }

@@ -149,9 +149,20 @@ def test_plan_misaligned_ld_copies_operand(lib):
 
 
 def test_plan_transposed_operands(lib):
+    # FFMA reads A M-major and B K-major only: transposed operands are copied transposed
     p = plan(300, 200, 100, "ffma", transa="T", transb="T")
     assert p["prep_a_name"] == "transpose" and p["prep_b_name"] == "transpose"
     assert p["ld_a"] == 300 and p["ld_b"] == 100
+    # the tensor-core kernels read either orientation in place
+    t = plan(300, 200, 100, "tf32", transa="T", transb="T", lda=104, ldb=204)
+    assert t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
+    assert t["ld_a"] == 104 and t["ld_b"] == 204 and t["launches"] == 1
+    # 3xTF32 splits them without transposing: ld is the stored row count rounded to 4
+    x = plan(300, 200, 101, "3xtf32", transa="T", transb="T")
+    assert x["prep_a_name"] == "split" and x["ld_a"] == 104 and x["ld_b"] == 200
+    # a misaligned transposed operand is copied (not transposed) for the tensor cores
+    c = plan(300, 200, 100, "tf32", transa="T", lda=101)
+    assert c["prep_a_name"] == "copy" and c["ld_a"] == 100
 
 
 def test_plan_trivial_cases(lib):

@@ -138,6 +138,22 @@ def test_transposed_operands(mode, trans):
     _assert_ok(H.check_problem(p, mode), "trans %s %s" % (trans, mode))
 
 
+@pytest.mark.parametrize("mode", ("tf32", "3xtf32"))
+@pytest.mark.parametrize("trans", ["NT", "TN", "TT"])
+@pytest.mark.parametrize("mnk", [(512, 384, 256), (96, 64, 1000), (1024, 96, 333), (640, 1024, 2048)])
+def test_transposed_operands_read_in_place(mode, trans, mnk):
+    """The tensor-core kernels read transposed operands through K-major / N-major
+    descriptors (3-D boxes when the extent is a multiple of 32) instead of a
+    transposing copy; covers the SM-pair and single-SM kernels."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, transa=trans[0], transb=trans[1], alpha=1.5, beta=-1.0, dist="normal", seed=31)
+    plan = pg.sgemm_plan(p.transa, p.transb, m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode)
+    if mode == "tf32":  # no transposing copy; an ld that is not a multiple of 4 still needs a plain copy
+        assert plan["prep_a_name"] == ("none" if p.lda % 4 == 0 else "copy")
+        assert plan["prep_b_name"] == ("none" if p.ldb % 4 == 0 else "copy")
+    _assert_ok(H.check_problem(p, mode), "in-place trans %s %s %s" % (trans, mode, mnk))
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
                                  (128, 256, 32), (257, 513, 1031), (64, 64, 200000), (160, 200, 300), (288, 130, 77),
