@@ -46,11 +46,16 @@
 namespace pg {
 namespace {
 
-template <int BN>
+// Columns per thread for the 128-wide tile (a compile-time tunable, 8 or 16).
+#ifndef PG_FFMA_JJ128
+#define PG_FFMA_JJ128 8
+#endif
+
+template <int BN, int JJ>
 struct FfmaCfg {
     static constexpr int BM = kBM;
     static constexpr int BK = kFfmaBK;
-    static constexpr int TGN = BN / 8;                    // thread columns
+    static constexpr int TGN = BN / JJ;                   // thread columns (JJ columns per thread)
     static constexpr int THREADS = 16 * TGN;              // 16 thread rows x TGN
     static constexpr int CWARPS = THREADS / 32;
     static constexpr int STAGES = (BN == 128) ? 3 : 4;
@@ -73,11 +78,11 @@ __device__ __forceinline__ float comp(const float4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <int BN>
-__global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM)
+template <int BN, int JJ>
+__global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTAS_PER_SM)
     ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams p) {
-    using Cfg = FfmaCfg<BN>;
+    using Cfg = FfmaCfg<BN, JJ>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
@@ -142,11 +147,11 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
 
     // acc[r][jj] holds rows (2r, 2r+1) of the thread's 8 rows {4tm..4tm+3, 64+4tm..64+4tm+3}
     // in column jj, as a register pair (the operand shape of the packed FP32 FMA).
-    float2 acc[4][8];
+    float2 acc[4][JJ];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+        for (int j = 0; j < JJ; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
 
     bool ok = true;
     for (int it = 0; it < nkb; ++it) {
@@ -166,10 +171,10 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
         const uint8_t* Bs = smem + s * Cfg::STAGE_BYTES + Cfg::A_BYTES + tn * 128;
 #pragma unroll
         for (int g2 = 0; g2 < Cfg::BK / 2; ++g2) {
-            float2 b[8];
+            float2 b[JJ];
             const uint32_t off2 = (((static_cast<uint32_t>(g2 >> 1)) ^ bchunk_xor) << 4) + ((g2 & 1) << 3);
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
+            for (int jj = 0; jj < JJ; ++jj)
                 b[jj] = *reinterpret_cast<const float2*>(Bs + jj * (Cfg::TGN * 128) + off2);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
                 const float2 a[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
                                      make_float2(a1.z, a1.w)};
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
+                for (int jj = 0; jj < JJ; ++jj) {
                     const float bv = kk == 0 ? b[jj].x : b[jj].y;
 #pragma unroll
                     for (int r = 0; r < 4; ++r) acc[r][jj] = __ffma2_rn(a[r], make_float2(bv, bv), acc[r][jj]);
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
     // ---------------- epilogue ----------------
     const float alpha = p.alpha, beta = p.beta;
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
+    for (int jj = 0; jj < JJ; ++jj) {
         const int64_t j = n0 + tn + Cfg::TGN * jj;
         if (j >= p.n) continue;
 #pragma unroll
@@ -241,11 +246,11 @@ __global__ void __launch_bounds__(FfmaCfg<BN>::THREADS, FfmaCfg<BN>::CTAS_PER_SM
     }
 }
 
-template <int BN>
+template <int BN, int JJ>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, dim3 grid,
                         cudaStream_t stream) {
-    using Cfg = FfmaCfg<BN>;
-    auto kern = ffma_gemm_kernel<BN>;
+    using Cfg = FfmaCfg<BN, JJ>;
+    auto kern = ffma_gemm_kernel<BN, JJ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
@@ -253,28 +258,25 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
     return cudaGetLastError();
 }
 
+using Cfg64 = FfmaCfg<64, 8>;
+using Cfg128 = FfmaCfg<128, PG_FFMA_JJ128>;
+using Cfg256 = FfmaCfg<256, 8>;
+
 }  // namespace
 
-int ffma_threads(int bn) {
-    return bn == 64 ? FfmaCfg<64>::THREADS : bn == 128 ? FfmaCfg<128>::THREADS : FfmaCfg<256>::THREADS;
-}
-int ffma_stages(int bn) {
-    return bn == 64 ? FfmaCfg<64>::STAGES : bn == 128 ? FfmaCfg<128>::STAGES : FfmaCfg<256>::STAGES;
-}
+int ffma_threads(int bn) { return bn == 64 ? Cfg64::THREADS : bn == 128 ? Cfg128::THREADS : Cfg256::THREADS; }
+int ffma_stages(int bn) { return bn == 64 ? Cfg64::STAGES : bn == 128 ? Cfg128::STAGES : Cfg256::STAGES; }
 int ffma_ctas_per_sm(int bn) {
-    return bn == 64 ? FfmaCfg<64>::CTAS_PER_SM
-                    : bn == 128 ? FfmaCfg<128>::CTAS_PER_SM : FfmaCfg<256>::CTAS_PER_SM;
+    return bn == 64 ? Cfg64::CTAS_PER_SM : bn == 128 ? Cfg128::CTAS_PER_SM : Cfg256::CTAS_PER_SM;
 }
-size_t ffma_smem_bytes(int bn) {
-    return bn == 64 ? FfmaCfg<64>::SMEM : bn == 128 ? FfmaCfg<128>::SMEM : FfmaCfg<256>::SMEM;
-}
+size_t ffma_smem_bytes(int bn) { return bn == 64 ? Cfg64::SMEM : bn == 128 ? Cfg128::SMEM : Cfg256::SMEM; }
 
 cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn,
                         dim3 grid, cudaStream_t stream) {
     switch (bn) {
-        case 64: return launch_impl<64>(tmA, tmB, p, grid, stream);
-        case 128: return launch_impl<128>(tmA, tmB, p, grid, stream);
-        case 256: return launch_impl<256>(tmA, tmB, p, grid, stream);
+        case 64: return launch_impl<64, 8>(tmA, tmB, p, grid, stream);
+        case 128: return launch_impl<128, PG_FFMA_JJ128>(tmA, tmB, p, grid, stream);
+        case 256: return launch_impl<256, 8>(tmA, tmB, p, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
