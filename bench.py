@@ -397,8 +397,14 @@ def main():
     ap.add_argument("--cpu-threads", type=int, default=0)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--fma-ceiling", action="store_true",
+                    help="run only the register-only FP32 FMA throughput probe and print its JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
+    if args.fma_ceiling:
+        from precision_gemm_gb300 import build as pgbuild
+        subprocess.run([pgbuild.build_probe()], check=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, args.workload)
     else:

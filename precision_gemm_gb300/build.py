@@ -71,5 +71,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+PROBE_SRC = os.path.join(HERE, "probes", "fma_ceiling.cu")
+PROBE_BIN = os.path.join(HERE, "probes", "fma_ceiling")
+
+
+def build_probe(force: bool = False) -> str:
+    """Compile the register-only FMA ceiling probe (a small executable)."""
+    if not force and os.path.exists(PROBE_BIN) and os.path.getmtime(PROBE_BIN) >= os.path.getmtime(PROBE_SRC):
+        return PROBE_BIN
+    subprocess.run([_nvcc(), *ARCH, "-O3", "-o", PROBE_BIN, PROBE_SRC], check=True)
+    return PROBE_BIN
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -398,17 +398,23 @@ struct Launcher {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::SMEM));
         if (e != cudaSuccess) return e;
-        // Pairs that can be resident at once (clusters must fit inside GPCs).
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2, 1, 1);
-        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-        cfg.dynamicSmemBytes = Cfg::SMEM;
-        cfg.stream = st;
-        int max_clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-        if (e != cudaSuccess || max_clusters <= 0) {
-            cudaGetLastError();
-            max_clusters = num_sms / 2;
+        // Pairs that can be resident at once (clusters must fit inside GPCs), asked
+        // once per device so a call captured into a CUDA graph only launches.
+        static int cached[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int max_clusters = (dev >= 0 && dev < 64) ? cached[dev] : 0;
+        if (max_clusters <= 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2, 1, 1);
+            cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+            cfg.dynamicSmemBytes = Cfg::SMEM;
+            e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+            if (e != cudaSuccess || max_clusters <= 0) {
+                cudaGetLastError();
+                max_clusters = num_sms / 2;
+            }
+            if (dev >= 0 && dev < 64) cached[dev] = max_clusters;
         }
         int pairs = units < max_clusters ? units : max_clusters;
         if (pairs < 1) pairs = 1;

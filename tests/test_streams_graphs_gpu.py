@@ -1,0 +1,91 @@
+"""Streams and CUDA graphs: the library's launches are stream-ordered and
+capturable once the stream's workspace has been sized by an ordinary call; a call
+that would have to grow the workspace during capture is refused with
+SGEMM_ERR_CAPTURE; concurrent calls on different streams use different
+workspaces and both stay correct."""
+import pytest
+import torch
+
+import oracle
+import precision_gemm_gb300 as pg
+from precision_gemm_gb300 import synth
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+MODES = ("ffma", "tf32", "3xtf32")
+
+
+@pytest.fixture(autouse=True)
+def _plain_plan():
+    pg.load_library()
+    pg.force_plan(0, 0)
+    yield
+    pg.force_plan(0, 0)
+
+
+def _check(p, mode, A, B, C, out):
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, out), cref, den, oracle.TOL[mode])
+    assert res["ok"], (mode, res)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_captured_call_replays_on_new_data(mode):
+    # split-K shape (workspace for partial sums) plus, for 3xTF32, the split operands
+    p = synth.Problem(256, 192, 8192, alpha=1.0, beta=0.5, dist="normal", seed=41)
+    A, B, C = synth.make(p)
+    s = torch.cuda.Stream()
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    with torch.cuda.stream(s):
+        pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)  # sizes workspace
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    A2, B2, C2 = synth.make(p.with_(seed=42))
+    dA.copy_(A2)
+    dB.copy_(B2)
+    dC.copy_(C2)
+    g.replay()
+    torch.cuda.synchronize()
+    _check(p, mode, A2, B2, C2, dC.cpu())
+    dC.copy_(C2)
+    g.replay()
+    torch.cuda.synchronize()
+    _check(p, mode, A2, B2, C2, dC.cpu())
+    assert pg.device_status() == 0
+
+
+def test_workspace_growth_during_capture_is_refused():
+    p = synth.Problem(256, 192, 8192, dist="normal", seed=43)
+    A, B, C = synth.make(p)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    s = torch.cuda.Stream()  # fresh stream: no workspace yet
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(pg.SgemmError) as e:
+        with torch.cuda.graph(g, stream=s):
+            pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, "3xtf32", s)
+    assert e.value.code == 7  # SGEMM_ERR_CAPTURE
+    torch.cuda.synchronize()
+    # the stream is usable afterwards
+    pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, "3xtf32", s)
+    torch.cuda.synchronize()
+    _check(p, "3xtf32", A, B, C, dC.cpu())
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_two_streams_run_concurrently(mode):
+    p1 = synth.Problem(1024, 768, 4096, alpha=1.0, beta=0.0, dist="normal", seed=51)
+    p2 = synth.Problem(640, 1280, 2048, alpha=2.0, beta=1.0, dist="normal", seed=52)
+    data = [synth.make(p) for p in (p1, p2)]
+    dev = [(A.cuda(), B.cuda(), C.cuda()) for A, B, C in data]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for p, (dA, dB, dC), (A, B, C), s in zip((p1, p2), dev, data, streams):
+            with torch.cuda.stream(s):
+                dC.copy_(C)  # ordered before the product on the same stream
+            pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    torch.cuda.synchronize()
+    for p, (dA, dB, dC), (A, B, C) in zip((p1, p2), dev, data):
+        _check(p, mode, A, B, C, dC.cpu())
