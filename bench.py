@@ -257,8 +257,10 @@ def run_ours(args, wl_name):
 
     # Dominant kernel: the mode whose launches take longest in the step.
     dom = max(modes, key=lambda m: mode_info[m]["ms_median"])
-    dom_kernel = {"ffma": "ffma_gemm_kernel", "tf32": "tc_gemm_kernel (tf32)", "3xtf32": "tc_gemm_kernel (3xtf32)"}[dom]
-    traffic = read_traffic(dom, wl_name)
+    kname = pg.sgemm_plan(p.transa, p.transb, p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc,
+                          dom, num_sms)["kernel_name"]
+    dom_kernel = "%s_gemm_kernel%s" % (kname, "" if dom == "ffma" else " (%s)" % dom)
+    traffic = read_traffic(dom, kname, wl_name)
     if dom == "ffma":
         roofline = {"bound": "alu", "achieved": mode_info[dom]["tflops"], "peak": fp32_peak, "unit": "TFLOP/s",
                     "frac": mode_info[dom]["tflops"] / fp32_peak,
@@ -292,13 +294,14 @@ def run_ours(args, wl_name):
     return line
 
 
-def read_traffic(mode: str, wl_name: str):
+def read_traffic(mode: str, kname: str, wl_name: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary
-    (profiles/<kernel>_<workload>.md: 'traffic_bytes_per_launch: N' plus the source
-    hash it was taken on); None when absent or taken on a different source."""
+    (profiles/<mode>_<workload>.md: 'traffic_bytes_per_launch: N' plus the hash of
+    the kernel source it was taken on); None when absent or taken on a different
+    source."""
     import hashlib
-    src = {"ffma": "ffma_kernel.cu"}.get(mode, "tc_kernel.cu")
-    path = os.path.join(ROOT, "profiles", "%s_%s.md" % ({"ffma": "ffma"}.get(mode, mode), wl_name))
+    src = "%s_kernel.cu" % kname
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (mode, wl_name))
     try:
         text = open(path).read()
     except OSError:

@@ -74,10 +74,6 @@ struct FfmaCfg {
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128B-swizzle slots need 1 KiB alignment");
 };
 
-__device__ __forceinline__ float comp(const float4& v, int i) {
-    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
 template <int BN, int JJ>
 __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTAS_PER_SM)
     ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -203,42 +199,71 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
     if (!ok || *abort_flag) return;
 
     // ---------------- epilogue ----------------
+    // C is read ahead of the stores, G columns of the thread's tile at a time:
+    // interleaved with the stores, each load would wait for the previous store
+    // (the compiler cannot rule out that they alias) at full DRAM latency.
     const float alpha = p.alpha, beta = p.beta;
+    const bool read_c = p.split == 1 && beta != 0.0f;
+    constexpr int G = JJ < 4 ? JJ : 4;
 #pragma unroll
-    for (int jj = 0; jj < JJ; ++jj) {
-        const int64_t j = n0 + tn + Cfg::TGN * jj;
-        if (j >= p.n) continue;
+    for (int j0 = 0; j0 < JJ; j0 += G) {
+        float4 cfr[G][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t i = m0 + 64 * h + 4 * tm;
-            if (i >= p.m) continue;
-            const float v[4] = {acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y};
-            if (p.split > 1) {
-                float* dst = p.P + slice * p.p_stride + j * p.ldp + i;
-                if (i + 3 < p.m) {
-                    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-                } else {
-                    for (int e = 0; e < 4; ++e)
-                        if (i + e < p.m) dst[e] = v[e];
+        for (int g = 0; g < G; ++g) {
+            const int64_t j = n0 + tn + Cfg::TGN * (j0 + g);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t i = m0 + 64 * h + 4 * tm;
+                const float* src = p.C + j * p.ldc + i;
+                float4 c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (read_c && j < p.n && i < p.m) {
+                    if (p.c_vec && i + 3 < p.m) {
+                        c = *reinterpret_cast<const float4*>(src);
+                    } else {
+                        c.x = src[0];
+                        if (i + 1 < p.m) c.y = src[1];
+                        if (i + 2 < p.m) c.z = src[2];
+                        if (i + 3 < p.m) c.w = src[3];
+                    }
                 }
-            } else {
-                float* dst = p.C + j * p.ldc + i;
-                if (p.c_vec && i + 3 < p.m) {
+                cfr[g][h] = c;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int jj = j0 + g;
+            const int64_t j = n0 + tn + Cfg::TGN * jj;
+            if (j >= p.n) continue;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t i = m0 + 64 * h + 4 * tm;
+                if (i >= p.m) continue;
+                const float v[4] = {acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y};
+                if (p.split > 1) {
+                    float* dst = p.P + slice * p.p_stride + j * p.ldp + i;
+                    if (i + 3 < p.m) {
+                        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+                        for (int e = 0; e < 4; ++e)
+                            if (i + e < p.m) dst[e] = v[e];
+                    }
+                } else {
+                    float* dst = p.C + j * p.ldc + i;
+                    const float4 c = cfr[g][h];
                     float4 o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
-                    if (beta != 0.0f) {
-                        const float4 c = *reinterpret_cast<const float4*>(dst);
+                    if (read_c) {
                         o.x = fmaf(beta, c.x, o.x);
                         o.y = fmaf(beta, c.y, o.y);
                         o.z = fmaf(beta, c.z, o.z);
                         o.w = fmaf(beta, c.w, o.w);
                     }
-                    *reinterpret_cast<float4*>(dst) = o;
-                } else {
-                    for (int e = 0; e < 4; ++e) {
-                        if (i + e >= p.m) break;
-                        float o = alpha * v[e];
-                        if (beta != 0.0f) o = fmaf(beta, dst[e], o);
-                        dst[e] = o;
+                    if (p.c_vec && i + 3 < p.m) {
+                        *reinterpret_cast<float4*>(dst) = o;
+                    } else {
+                        dst[0] = o.x;
+                        if (i + 1 < p.m) dst[1] = o.y;
+                        if (i + 2 < p.m) dst[2] = o.z;
+                        if (i + 3 < p.m) dst[3] = o.w;
                     }
                 }
             }

@@ -227,11 +227,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t bar = full_leader0 + 8 * s;
                     const int32_t kc = (kb0 + kb) * Cfg::BK;
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
-                    // A: one 3-D box {32 rows, BK, 4 row groups} when m % 32 == 0, else four
-                    // 2-D boxes of 32 rows (both land as 4 x [BK][32] row groups).
-                    // A K-major (transa 'T'): one box of 128 rows x BK; A M-major: one 3-D box
-                    // or four 2-D boxes of 32 rows.  B K-major: one box of BN/2 columns;
-                    // B N-major (transb 'T'): BN/64 groups of 32 columns.
+                    // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
+                    // box {32 rows, BK, 4 row groups} when m % 32 == 0, else four 2-D boxes
+                    // of 32 rows (both land as 4 x [BK][32] row groups).  B K-major: one box
+                    // of BN/2 columns; B N-major (transb 'T'): BN/64 groups of 32 columns.
                     auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
                         if (p.a_kmajor) {
                             tma_load_2d_pair(dst, map, kc, ma, bar);
@@ -351,23 +350,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             for (int c = 0; c < BN / 32; ++c) {
                 const int64_t jb = n0 + 32 * c;
                 if (jb >= p.n) break;  // uniform across the warp
+                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
+                // All 32 loads of C are issued before the tensor-memory read and
+                // before any store: interleaved with the stores, each load would wait
+                // for the previous store (the compiler cannot rule out that they
+                // alias) and the epilogue would run at DRAM latency.
+                float* dst = p.C + jb * p.ldc + i;
+                const bool read_c = row_ok && p.split == 1 && beta != 0.0f;
+                float cv[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_base + 32 * c, v);
                 tmem_wait_ld();
                 if (!row_ok) continue;
-                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
                 if (p.split > 1) {
-                    float* dst = p.P + slice * p.p_stride + jb * p.ldp + i;
+                    float* part = p.P + slice * p.p_stride + jb * p.ldp + i;
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        if (t < jn) dst[t * p.ldp] = __uint_as_float(v[t]);
+                        if (t < jn) part[t * p.ldp] = __uint_as_float(v[t]);
                 } else {
-                    float* dst = p.C + jb * p.ldc + i;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         if (t < jn) {
                             float o = alpha * __uint_as_float(v[t]);
-                            if (beta != 0.0f) o = fmaf(beta, dst[t * p.ldc], o);
+                            if (beta != 0.0f) o = fmaf(beta, cv[t], o);
                             dst[t * p.ldc] = o;
                         }
                     }

@@ -232,23 +232,31 @@ __global__ void __launch_bounds__(192, 1)
             for (int c = 0; c < BN / 32; ++c) {
                 const int64_t jb = n0 + 32 * c;
                 if (jb >= p.n) break;  // uniform across the warp
+                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
+                // All 32 loads of C are issued before the tensor-memory read and
+                // before any store: interleaved with the stores, each load would wait
+                // for the previous store (the compiler cannot rule out that they
+                // alias) and the epilogue would run at DRAM latency.
+                float* dst = p.C + jb * p.ldc + i;
+                const bool read_c = row_ok && p.split == 1 && beta != 0.0f;
+                float cv[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_base + 32 * c, v);
                 tmem_wait_ld();
                 if (!row_ok) continue;
-                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
                 if (p.split > 1) {
-                    float* dst = p.P + slice * p.p_stride + jb * p.ldp + i;
+                    float* part = p.P + slice * p.p_stride + jb * p.ldp + i;
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        if (t < jn) dst[t * p.ldp] = __uint_as_float(v[t]);
+                        if (t < jn) part[t * p.ldp] = __uint_as_float(v[t]);
                 } else {
-                    float* dst = p.C + jb * p.ldc + i;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         if (t < jn) {
                             float o = alpha * __uint_as_float(v[t]);
-                            if (beta != 0.0f) o = fmaf(beta, dst[t * p.ldc], o);
+                            if (beta != 0.0f) o = fmaf(beta, cv[t], o);
                             dst[t * p.ldc] = o;
                         }
                     }

@@ -154,6 +154,31 @@ def test_transposed_operands_read_in_place(mode, trans, mnk):
     _assert_ok(H.check_problem(p, mode), "in-place trans %s %s %s" % (trans, mode, mnk))
 
 
+@pytest.mark.parametrize("mode", ("tf32", "3xtf32"))
+@pytest.mark.parametrize("trans", ["NN", "NT", "TN", "TT"])
+@pytest.mark.parametrize("case", [
+    # (m, n, k, forced bn): SM-pair tiles with ragged rows/columns and split-K
+    (1024, 1024, 512, 0),
+    (700, 2148, 300, 0),
+    (640, 640, 1000, 0),
+    (1000, 512, 777, 128),   # 128-wide pair tiles, 2-D A boxes when M-major
+    (512, 512, 8192, 0),     # split-K on the pair kernel
+])
+def test_pair_kernel_shapes(mode, trans, case):
+    """The SM-pair kernel (256-row tiles) with every operand orientation,
+    ragged edges, both tile widths, and split-K; beta != 0 so the epilogue's
+    batched reads of C are checked."""
+    m, n, k, bn = case
+    p = synth.Problem(m, n, k, transa=trans[0], transb=trans[1], alpha=0.75, beta=1.5, dist="normal", seed=37)
+    try:
+        pg.force_plan(bn, 0)
+        plan = pg.sgemm_plan(p.transa, p.transb, m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode)
+        assert plan["kernel_name"] == "tc2", plan
+        _assert_ok(H.check_problem(p, mode), "pair %s %s %s" % (case, trans, mode))
+    finally:
+        pg.force_plan(0, 0)
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
                                  (128, 256, 32), (257, 513, 1031), (64, 64, 200000), (160, 200, 300), (288, 130, 77),
