@@ -36,28 +36,89 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
     small = x - b;
 }
 
-// dst(r, c) = src(r, c), r < rows, c < cols; one warp row-stride per column.
-template <bool SPLIT>
-__global__ void __launch_bounds__(256) prep_copy_kernel(const float* __restrict__ src, int64_t lds,
-                                                        int64_t rows, int64_t cols, float* __restrict__ dst,
-                                                        float* __restrict__ dst_small, int64_t ldd) {
-    for (int64_t c = blockIdx.y; c < cols; c += gridDim.y) {
-        const float* s = src + c * lds;
-        float* d = dst + c * ldd;
-        float* ds = SPLIT ? dst_small + c * ldd : nullptr;
-        for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < rows;
-             r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-            const float x = s[r];
-            if (SPLIT) {
-                float b, sm;
-                split_tf32(x, b, sm);
-                d[r] = b;
-                ds[r] = sm;
-            } else {
-                d[r] = x;
+// Column sweep over a column-major rows x cols matrix: a CTA of 256 threads
+// covers TX = 2^tx_shift consecutive rows (32 <= TX <= 256, the smallest power of
+// two >= rows) of 256 / TX columns, so a narrow matrix keeps every lane busy and
+// every warp still touches 128 contiguous bytes.  A thread issues kU loads before
+// any store -- kU of its columns, or, when it owns fewer than kU columns, kU of
+// its rows (by_rows) -- because a thread whose loads wait on its own earlier
+// stores keeps a single load in flight.
+constexpr int kU = 8;
+
+struct Sweep {
+    int tx, ty;        // this thread's row / column offset inside the CTA's block
+    int TX, TY;        // rows and columns one CTA covers per step
+    int64_t rstep;     // row distance between a thread's consecutive rows
+    int64_t cstep;     // column distance between a thread's consecutive columns
+};
+
+__device__ __forceinline__ Sweep sweep_setup(int tx_shift) {
+    Sweep w;
+    w.TX = 1 << tx_shift;
+    w.TY = 256 >> tx_shift;
+    w.tx = threadIdx.x & (w.TX - 1);
+    w.ty = threadIdx.x >> tx_shift;
+    w.rstep = static_cast<int64_t>(gridDim.x) * w.TX;
+    w.cstep = static_cast<int64_t>(gridDim.y) * w.TY;
+    return w;
+}
+
+// Visit every (r, c) of the sweep in batches of up to kU positions of one thread:
+// f_load(batch index, r, c) for the whole batch, then f_store(batch index, r, c).
+template <class Load, class Store>
+__device__ __forceinline__ void sweep_batches(const Sweep& w, int64_t rows, int64_t cols, bool by_rows,
+                                              Load&& f_load, Store&& f_store) {
+    const int64_t r_first = static_cast<int64_t>(blockIdx.x) * w.TX + w.tx;
+    const int64_t c_first = static_cast<int64_t>(blockIdx.y) * w.TY + w.ty;
+    if (by_rows) {
+        for (int64_t c = c_first; c < cols; c += w.cstep) {
+            for (int64_t r0 = r_first; r0 < rows; r0 += kU * w.rstep) {
+                const int64_t left = (rows - r0 + w.rstep - 1) / w.rstep;
+                const int nu = left < kU ? static_cast<int>(left) : kU;
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    if (u < nu) f_load(u, r0 + u * w.rstep, c);
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    if (u < nu) f_store(u, r0 + u * w.rstep, c);
+            }
+        }
+    } else {
+        for (int64_t r = r_first; r < rows; r += w.rstep) {
+            for (int64_t c0 = c_first; c0 < cols; c0 += kU * w.cstep) {
+                const int64_t left = (cols - c0 + w.cstep - 1) / w.cstep;
+                const int nu = left < kU ? static_cast<int>(left) : kU;
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    if (u < nu) f_load(u, r, c0 + u * w.cstep);
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    if (u < nu) f_store(u, r, c0 + u * w.cstep);
             }
         }
     }
+}
+
+// dst(r, c) = src(r, c), r < rows, c < cols (and the TF32 split when SPLIT).
+template <bool SPLIT>
+__global__ void __launch_bounds__(256, SPLIT ? 3 : 4)
+    prep_copy_kernel(const float* __restrict__ src, int64_t lds, int64_t rows, int64_t cols,
+                     float* __restrict__ dst, float* __restrict__ dst_small, int64_t ldd, int tx_shift,
+                     int by_rows) {
+    const Sweep w = sweep_setup(tx_shift);
+    float x[kU];
+    sweep_batches(
+        w, rows, cols, by_rows != 0, [&](int u, int64_t r, int64_t c) { x[u] = src[c * lds + r]; },
+        [&](int u, int64_t r, int64_t c) {
+            if (SPLIT) {
+                float b, sm;
+                split_tf32(x[u], b, sm);
+                dst[c * ldd + r] = b;
+                dst_small[c * ldd + r] = sm;
+            } else {
+                dst[c * ldd + r] = x[u];
+            }
+        });
 }
 
 // dst(r, c) = src(c, r): 32 x 32 tiles through shared memory so that both the
@@ -97,42 +158,69 @@ __global__ void __launch_bounds__(256) prep_transpose_kernel(const float* __rest
     }
 }
 
-// C = alpha * sum_{s < split} P[s] + beta * C over the m x n output.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p) {
-    for (int64_t j = blockIdx.y; j < p.n; j += gridDim.y) {
-        const float* pj = p.P + j * p.ldp;
-        float* cj = p.C + j * p.ldc;
-        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.m;
-             i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+// C = alpha * sum_{s < split} P[s] + beta * C over the m x n output; every
+// output sums its slices in increasing s.  Loads run kS slices ahead of the
+// additions, so kS loads are in flight per output even when a thread owns one.
+constexpr int kS = 8;
+
+__global__ void __launch_bounds__(256, 4) splitk_reduce_kernel(const GemmParams p, int tx_shift) {
+    const Sweep w = sweep_setup(tx_shift);
+    const float* __restrict__ P = p.P;
+    float* __restrict__ C = p.C;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * w.TX + w.tx; r < p.m; r += w.rstep) {
+        for (int64_t c = static_cast<int64_t>(blockIdx.y) * w.TY + w.ty; c < p.n; c += w.cstep) {
+            const float* ps = P + c * p.ldp + r;
+            const float cin = p.beta != 0.0f ? C[c * p.ldc + r] : 0.0f;
             float acc = 0.0f;
-            for (int s = 0; s < p.split; ++s) acc += pj[s * p.p_stride + i];
+            int s = 0;
+            for (; s + kS <= p.split; s += kS) {
+                float v[kS];
+#pragma unroll
+                for (int j = 0; j < kS; ++j) v[j] = ps[(s + j) * p.p_stride];
+#pragma unroll
+                for (int j = 0; j < kS; ++j) acc += v[j];
+            }
+            for (; s < p.split; ++s) acc += ps[s * p.p_stride];
             float o = p.alpha * acc;
-            if (p.beta != 0.0f) o = fmaf(p.beta, cj[i], o);
-            cj[i] = o;
+            if (p.beta != 0.0f) o = fmaf(p.beta, cin, o);
+            C[c * p.ldc + r] = o;
         }
     }
 }
 
-__global__ void __launch_bounds__(256) scale_kernel(float* __restrict__ C, int64_t ldc, int64_t m, int64_t n,
-                                                    float beta) {
-    for (int64_t j = blockIdx.y; j < n; j += gridDim.y) {
-        float* cj = C + j * ldc;
-        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < m;
-             i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-            cj[i] = (beta == 0.0f) ? 0.0f : beta * cj[i];
-    }
+// C = beta * C (beta = 0 writes zeros without reading C).
+__global__ void __launch_bounds__(256, 4) scale_kernel(float* __restrict__ C, int64_t ldc, int64_t m, int64_t n,
+                                                       float beta, int tx_shift, int by_rows) {
+    const Sweep w = sweep_setup(tx_shift);
+    float x[kU];
+    sweep_batches(
+        w, m, n, by_rows != 0,
+        [&](int u, int64_t r, int64_t c) { x[u] = beta != 0.0f ? C[c * ldc + r] : 0.0f; },
+        [&](int u, int64_t r, int64_t c) { C[c * ldc + r] = (beta == 0.0f) ? 0.0f : beta * x[u]; });
 }
 
-// Column-sweep grid: x covers rows (256 threads each), y covers columns; the
-// total is a multiple of the SM count, capped so each CTA loops a few times.
-dim3 column_grid(int64_t rows, int64_t cols, int num_sms) {
-    const int64_t bx = (rows + 255) / 256;
-    const int64_t bx_c = bx < 8 ? bx : 8;
-    int64_t by = (static_cast<int64_t>(num_sms) * 8 + bx_c - 1) / bx_c;
-    if (by > cols) by = cols;
+// Grid of the column sweep: about 8 CTAs per SM; y spans column groups of
+// 256 / TX columns first, x then spans row blocks.  *by_rows tells the kernel
+// to batch a thread's rows when it owns fewer than kU columns.
+dim3 sweep_grid(int64_t rows, int64_t cols, int num_sms, int* tx_shift, int* by_rows) {
+    int sh = 5;
+    while (sh < 8 && (int64_t(1) << sh) < rows) ++sh;
+    *tx_shift = sh;
+    const int64_t TX = int64_t(1) << sh, TY = 256 >> sh;
+    const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+    const int64_t col_groups = (cols + TY - 1) / TY;
+    const int64_t row_blocks = (rows + TX - 1) / TX;
+    int64_t by = col_groups < target ? col_groups : target;
     if (by > 65535) by = 65535;
     if (by < 1) by = 1;
-    return dim3(static_cast<unsigned>(bx_c < 1 ? 1 : bx_c), static_cast<unsigned>(by));
+    int64_t bx = (target + by - 1) / by;
+    if (bx > row_blocks) bx = row_blocks;
+    if (bx > 65535) bx = 65535;
+    if (bx < 1) bx = 1;
+    const int64_t cols_per_thread = (cols + by * TY - 1) / (by * TY);
+    const int64_t rows_per_thread = (rows + bx * TX - 1) / (bx * TX);
+    *by_rows = (cols_per_thread < kU && rows_per_thread > cols_per_thread) ? 1 : 0;
+    return dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by));
 }
 
 }  // namespace
@@ -152,23 +240,29 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
             prep_transpose_kernel<false><<<static_cast<unsigned>(g), block, 0, stream>>>(src, lds, rows, cols,
                                                                                          dst, nullptr, ldd);
     } else {
-        const dim3 grid = column_grid(rows, cols, num_sms);
+        int sh = 8, by_rows = 0;
+        const dim3 grid = sweep_grid(rows, cols, num_sms, &sh, &by_rows);
         if (dst_small)
-            prep_copy_kernel<true><<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, dst_small, ldd);
+            prep_copy_kernel<true>
+                <<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, dst_small, ldd, sh, by_rows);
         else
-            prep_copy_kernel<false><<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, nullptr, ldd);
+            prep_copy_kernel<false><<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, nullptr, ldd, sh, by_rows);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t stream) {
-    splitk_reduce_kernel<<<column_grid(p.m, p.n, num_sms), 256, 0, stream>>>(p);
+    int sh = 8, by_rows = 0;
+    const dim3 grid = sweep_grid(p.m, p.n, num_sms, &sh, &by_rows);
+    splitk_reduce_kernel<<<grid, 256, 0, stream>>>(p, sh);
     return cudaGetLastError();
 }
 
 cudaError_t launch_scale(float* C, int64_t ldc, int64_t m, int64_t n, float beta, int num_sms,
                          cudaStream_t stream) {
-    scale_kernel<<<column_grid(m, n, num_sms), 256, 0, stream>>>(C, ldc, m, n, beta);
+    int sh = 8, by_rows = 0;
+    const dim3 grid = sweep_grid(m, n, num_sms, &sh, &by_rows);
+    scale_kernel<<<grid, 256, 0, stream>>>(C, ldc, m, n, beta, sh, by_rows);
     return cudaGetLastError();
 }
 

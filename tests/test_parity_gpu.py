@@ -227,6 +227,29 @@ def test_alpha_zero_and_k_zero(mode):
     assert torch.equal(out1.view(torch.int32), C.view(torch.int32))
 
 
+@pytest.mark.parametrize("shape", [(70001, 5), (100, 3000), (33, 1)])
+def test_scale_sweep_shapes(shape):
+    """C = beta*C (alpha = 0) over tall, wide and tiny C: the sweep batches a
+    thread's rows when it owns fewer columns than its batch, else its columns."""
+    m, n = shape
+    p = synth.Problem(m, n, 3, ldc=m + 3, alpha=0.0, beta=-1.25, dist="normal", seed=23)
+    A, B, C = synth.make(p)
+    out, ok = H.run_gpu(p, "tf32", A, B, C)
+    assert ok and H.padding_intact(p, out, C)
+    expect = np.float32(-1.25) * H.logical(p, C).astype(np.float32)  # one fp32 rounding, as on the GPU
+    assert np.array_equal(H.logical(p, out), expect.astype(np.float64))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mnk", [(96, 3, 50000), (5000, 3, 70), (130, 130, 100000)])
+def test_split_prep_and_reduce_shapes(mode, mnk):
+    """Operand copies / TF32 splits of tall-narrow and short-wide operands, and
+    split-K reductions over many slices, against the oracle (beta != 0)."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, lda=m + 1, ldb=k + 1, ldc=m + 2, alpha=1.5, beta=0.5, dist="normal", seed=29)
+    _assert_ok(H.check_problem(p, mode), "%s %s" % (mnk, mode))
+
+
 def test_empty_sizes_are_no_ops():
     C = torch.full((16,), 3.0, device="cuda")
     pg.sgemm("N", "N", 0, 4, 4, 1.0, None, 1, None, 4, 0.0, C, 1)
