@@ -61,6 +61,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUt
 // tcgen05 kernel on SM pairs (cta_group::2, persistent, double-buffered TMEM):
 // pair tile 256 x bn, bn in {128, 256}; launches min(units, resident pairs) pairs.
 int tc2_bk(bool split3);
+int tc2_threads();
 int tc2_stages(int bn, bool split3);
 size_t tc2_smem_bytes(int bn, bool split3);
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,

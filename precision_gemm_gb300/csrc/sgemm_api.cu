@@ -159,7 +159,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->bm = pair ? 2 * kBM : kBM;
     pl->bk = !tc ? kFfmaBK : (pair ? tc2_bk(split3) : tc_bk(split3));
     pl->stages = !tc ? ffma_stages(bn) : (pair ? tc2_stages(bn, split3) : tc_stages(bn, split3));
-    pl->threads = tc ? tc_threads() : ffma_threads(bn);
+    pl->threads = !tc ? ffma_threads(bn) : (pair ? tc2_threads() : tc_threads());
     pl->ctas_per_sm = tc ? 1 : ffma_ctas_per_sm(bn);
     pl->smem_bytes = !tc ? ffma_smem_bytes(bn) : (pair ? tc2_smem_bytes(bn, split3) : tc_smem_bytes(bn, split3));
     pl->tiles_m = static_cast<int>(cdiv(m, pl->bm));

@@ -13,14 +13,17 @@
 // static stride, and the accumulator is double-buffered in TMEM (2 x BN columns)
 // so the epilogue of one unit overlaps the MMAs of the next.
 //
-// Warp roles, in both CTAs of the pair (192 threads each):
+// Warp roles, in both CTAs of the pair (320 threads each):
 //   warp 0      TMA loader: this CTA's A rows and B columns for every k-block,
 //               completing on CTA 0's "full" barrier of the ring slot
 //   warp 1      TMEM allocation (pair-wide); in CTA 0 one thread issues the MMAs
-//   warps 2-5   epilogue: TMEM -> registers -> alpha/beta -> C rows of this CTA
+//   warps 2-9   epilogue: TMEM -> registers -> alpha/beta -> C rows of this CTA;
+//               a warp may read only TMEM lane quarter (warp % 4), so two warps
+//               share each quarter and take alternate 32-column chunks (with one
+//               warp per quarter the epilogue is issue-bound when K is short)
 // Barriers: full[s] (CTA 0: expect-tx for both CTAs' bytes), empty[s] (both CTAs;
 // the MMA completion is multicast), acc_full[b] (both CTAs; multicast),
-// acc_empty[b] (CTA 0; arrived by the 8 epilogue warps of the pair).
+// acc_empty[b] (CTA 0; arrived by the 16 epilogue warps of the pair).
 //
 // Shared-memory layouts are those of the single-SM kernel (tc_kernel.cu): A
 // M-major in the 128-byte swizzle with 32-byte atoms, B K-major in the 128-byte
@@ -124,7 +127,13 @@ struct Tc2Cfg {
     static constexpr int STAGE_BYTES = OPS * (A_BYTES + B_BYTES);
     static constexpr int STAGES_RAW = (PG_TC2_RING_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
-    static constexpr int THREADS = 192;
+// Epilogue warps (a compile-time tunable: 4 or 8).
+#ifndef PG_TC2_EPI_WARPS
+#define PG_TC2_EPI_WARPS 8
+#endif
+    static constexpr int EPI_WARPS = PG_TC2_EPI_WARPS;
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulator buffers
@@ -134,7 +143,7 @@ struct Tc2Cfg {
 };
 
 template <int BN, bool SPLIT3>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
                     const GemmParams p) {
@@ -168,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full0 + 8 * b, 1);
-            mbar_init(acc_empty0 + 8 * b, 8);
+            mbar_init(acc_empty0 + 8 * b, 2 * Cfg::EPI_WARPS);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -326,8 +335,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ---------------- epilogue (warps 2..9, both CTAs) ----------------
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        constexpr int kGroups = Cfg::EPI_WARPS / 4;  // warps sharing a lane quarter
+        const int half = (warp - 2) >> 2;            // which of their 32-column chunks it takes
         const uint32_t acc_empty_leader0 = map_to_rank(acc_empty0, 0);
         const float alpha = p.alpha, beta = p.beta;
         int lu = 0;
@@ -347,10 +358,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             const bool row_ok = i < p.m;
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = half; c < BN / 32; c += kGroups) {
                 const int64_t jb = n0 + 32 * c;
                 if (jb >= p.n) break;  // uniform across the warp
-                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
+                const bool full = p.n - jb >= 32;
+                const int jn = full ? 32 : static_cast<int>(p.n - jb);
                 // All 32 loads of C are issued before the tensor-memory read and
                 // before any store: interleaved with the stores, each load would wait
                 // for the previous store (the compiler cannot rule out that they
@@ -358,8 +370,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 float* dst = p.C + jb * p.ldc + i;
                 const bool read_c = row_ok && p.split == 1 && beta != 0.0f;
                 float cv[32];
+                if (read_c && full) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
+                    for (int t = 0; t < 32; ++t) cv[t] = dst[t * p.ldc];
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
+                }
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_base + 32 * c, v);
                 tmem_wait_ld();
@@ -369,6 +386,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
                         if (t < jn) part[t * p.ldp] = __uint_as_float(v[t]);
+                } else if (full) {
+                    // whole chunk: no per-column predicate; beta == 0 reads nothing
+                    if (beta == 0.0f) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) dst[t * p.ldc] = alpha * __uint_as_float(v[t]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) dst[t * p.ldc] = fmaf(beta, cv[t], alpha * __uint_as_float(v[t]));
+                    }
                 } else {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
@@ -434,6 +460,8 @@ struct Launcher {
 }  // namespace
 
 int tc2_bk(bool split3) { return split3 ? Tc2Cfg<256, true>::BK : Tc2Cfg<256, false>::BK; }
+
+int tc2_threads() { return Tc2Cfg<256, false>::THREADS; }
 
 int tc2_stages(int bn, bool split3) {
     if (split3) return bn == 128 ? Tc2Cfg<128, true>::STAGES : Tc2Cfg<256, true>::STAGES;
