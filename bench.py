@@ -197,22 +197,31 @@ def run_ours(args, wl_name):
     total_ms = float(t.item())
 
     # End to end through the public host-buffer entry point: pinned host inputs,
-    # every step copies A, B (and Cin when beta != 0) in and C out.
+    # every step copies A, B (and Cin when beta != 0) in and C out for each mode.
+    # The modes' calls are queued with sgemm_host_async on one stream each, so one
+    # call's copies overlap another's arithmetic; the step ends when all are done.
     e2e = None
     if not args.skip_e2e:
         hA, hB = A.pin_memory(), B.pin_memory()
-        hC = C.clone().pin_memory()
+        hCs = {mode: C.clone().pin_memory() for mode in modes}  # each call reads and writes its own C
+        hstreams = {mode: torch.cuda.Stream() for mode in modes}
         h2d = (A.numel() + B.numel() + (C.numel() if p.beta != 0 else 0)) * 4 * len(modes)
         d2h = p.m * p.n * 4 * len(modes)
 
         def host_step():
+            go = torch.cuda.Event()
+            go.record(stream)
             for mode in modes:
+                s = hstreams[mode]
+                s.wait_event(go)
                 if p.layout == "col":
-                    pg.sgemm_host(p.transa, p.transb, p.m, p.n, p.k, p.alpha, hA, p.lda, hB, p.ldb, p.beta, hC,
-                                  p.ldc, mode, stream)
+                    pg.sgemm_host_async(p.transa, p.transb, p.m, p.n, p.k, p.alpha, hA, p.lda, hB, p.ldb, p.beta,
+                                        hCs[mode], p.ldc, mode, s)
                 else:
-                    pg.sgemm_host("N", "N", p.n, p.m, p.k, p.alpha, hB, p.ldb, hA, p.lda, p.beta, hC, p.ldc,
-                                  mode, stream)
+                    pg.sgemm_host_async("N", "N", p.n, p.m, p.k, p.alpha, hB, p.ldb, hA, p.lda, p.beta, hCs[mode],
+                                        p.ldc, mode, s)
+            for mode in modes:
+                stream.wait_stream(hstreams[mode])
         for _ in range(max(1, min(args.warmup, 2))):
             host_step()
         e_steps = max(1, min(args.steps, 3))
@@ -230,7 +239,7 @@ def run_ours(args, wl_name):
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
         e2e = {"value": world * flops * len(modes) / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-               "api": "sgemm_host (pinned host buffers)"}
+               "api": "sgemm_host_async, one stream per mode (pinned host buffers)"}
 
     if rank != 0:
         if dist:

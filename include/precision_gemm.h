@@ -126,6 +126,22 @@ int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
                float *C, int64_t ldc, int mode, void *stream);
 
 /*
+ * sgemm_host_async -- sgemm_host without the final synchronisation: the
+ * copies in, the product and the copy of C out are queued in `stream` order
+ * (after the work already queued on `stream`) and the call returns; C holds
+ * the result once `stream` has been synchronised (or an event recorded on it
+ * after the call has completed).  Until then the caller must not write A, B
+ * or C, nor read C.  Calls on different streams overlap one call's copies
+ * with another's arithmetic (the host link and the SMs are separate
+ * resources).  With page-locked (pinned) host arrays the call does not wait;
+ * with pageable arrays the CUDA runtime may block in the copies.  Returns as
+ * sgemm_host; an error detected after queueing is reported by the stream.
+ */
+int sgemm_host_async(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                     float *C, int64_t ldc, int mode, void *stream);
+
+/*
  * sgemm_noalloc -- sgemm without any device allocation.  (The pages have no
  * counterpart: this entry exists for callers of this library, not for the
  * method.)

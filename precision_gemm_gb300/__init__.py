@@ -35,9 +35,9 @@ KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc", 4: "tc2"}
 PREPS = {0: "none", 1: "copy", 2: "transpose", 3: "split"}
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTS = ("sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_plan", "sgemm_device_status", "sgemm_set_wait_timeout",
-           "sgemm_force_plan", "sgemm_debug_flags", "sgemm_launch_count", "sgemm_workspace_release",
-           "sgemm_last_error_string", "sgemm_version")
+EXPORTS = ("sgemm", "sgemm_host", "sgemm_host_async", "sgemm_noalloc", "sgemm_plan", "sgemm_device_status",
+           "sgemm_set_wait_timeout", "sgemm_force_plan", "sgemm_debug_flags", "sgemm_launch_count",
+           "sgemm_workspace_release", "sgemm_last_error_string", "sgemm_version")
 
 
 class SgemmError(RuntimeError):
@@ -78,6 +78,8 @@ def load_library(path: str | None = None):
         lib.sgemm.restype = i
         lib.sgemm_host.argtypes = gemm_args
         lib.sgemm_host.restype = i
+        lib.sgemm_host_async.argtypes = gemm_args
+        lib.sgemm_host_async.restype = i
         lib.sgemm_noalloc.argtypes = gemm_args
         lib.sgemm_noalloc.restype = i
         lib.sgemm_plan.argtypes = gemm_args[:14] + [i, ctypes.POINTER(sgemm_plan_t)]
@@ -151,6 +153,15 @@ def sgemm_host(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mod
     lib = load_library()
     _check(lib.sgemm_host(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                           _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
+
+
+def sgemm_host_async(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma",
+                     stream=None) -> None:
+    """sgemm_host queued on `stream` without waiting: C holds the result once the
+    stream is synchronised; until then A, B and C must stay untouched (and alive)."""
+    lib = load_library()
+    _check(lib.sgemm_host_async(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                                _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
 
 
 def sgemm_noalloc(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma",

@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -406,8 +407,42 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
 
 // ---- the call ---------------------------------------------------------------------------
 
+// Operand A already in the layout a plan's kernel reads (copied, transposed or
+// TF32-split once by a caller that runs several products on the same A, as
+// sgemm_host does for its column slabs).
+struct PreparedA {
+    const float* big = nullptr;
+    const float* small = nullptr;  // 3xTF32 remainder part
+};
+
+// Device bytes of A's preparation under plan pl (0 when A is read in place).
+size_t prep_a_bytes(const sgemm_plan_t& pl, char transa, int64_t m, int64_t k) {
+    if (pl.prep_a == SGEMM_PREP_NONE) return 0;
+    const int parts = pl.mode == SGEMM_3XTF32 ? 2 : 1;
+    const int64_t cols_a = (pl.kernel != SGEMM_KERNEL_FFMA && !is_notrans(transa)) ? m : k;
+    return parts * region(pl.ld_a * cols_a);
+}
+
+// Prepare A as plan pl asks into dst (prep_a_bytes(pl, ...) bytes); one launch.
+int prepare_a(const sgemm_plan_t& pl, char transa, int64_t m, int64_t k, const float* A, int64_t lda, char* dst,
+              int num_sms, cudaStream_t st, PreparedA* out) {
+    const int parts = pl.mode == SGEMM_3XTF32 ? 2 : 1;
+    float* d = reinterpret_cast<float*>(dst);
+    float* ds2 = parts == 2 ? reinterpret_cast<float*>(dst + prep_a_bytes(pl, transa, m, k) / 2) : nullptr;
+    const bool tr = pl.prep_a == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into M-major
+    const bool kmaj = !tr && !is_notrans(transa);      // tensor cores: stored k x m, kept as is
+    cudaError_t e = launch_prep(A, lda, tr, kmaj ? k : m, kmaj ? m : k, d, ds2, pl.ld_a, num_sms, st);
+    if (e != cudaSuccess) return fail_cuda(e, "operand preparation (A)");
+    out->big = d;
+    out->small = ds2;
+    return 0;
+}
+
+// pre != null: A is already prepared as this call's plan asks (same mode, transa,
+// m and k); the call then neither prepares A nor reserves workspace for it.
 int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
-        const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode, cudaStream_t st) {
+        const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode, cudaStream_t st,
+        const PreparedA* pre = nullptr) {
     int dev;
     DeviceState* ds;
     int rc = current_device(&dev, &ds);
@@ -421,6 +456,12 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
         g_launches += 1;
         return 0;
     }
+    const size_t a_prep = prep_a_bytes(pl, transa, m, k);
+    const bool a_given = pre != nullptr && a_prep > 0;
+    if (a_given) {
+        pl.workspace_bytes -= a_prep;
+        pl.launches -= 1;
+    }
     void* ws = nullptr;
     if ((rc = get_buffer(dev, st, kPurposeWorkspace, pl.workspace_bytes, &ws))) return rc;
     const bool split3 = mode == SGEMM_3XTF32;
@@ -429,21 +470,15 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
 
     const float* a_big = A;
     const float* a_small = nullptr;
-    if (pl.prep_a != SGEMM_PREP_NONE) {
-        float* d = reinterpret_cast<float*>(cursor);
-        const int64_t cols_a = (pl.kernel != SGEMM_KERNEL_FFMA && !is_notrans(transa)) ? m : k;
-        cursor += region(pl.ld_a * cols_a);
-        float* ds2 = nullptr;
-        if (parts == 2) {
-            ds2 = reinterpret_cast<float*>(cursor);
-            cursor += region(pl.ld_a * cols_a);
-        }
-        const bool tr = pl.prep_a == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into M-major
-        const bool kmaj = !tr && !is_notrans(transa);      // tensor cores: stored k x m, kept as is
-        if ((e = launch_prep(A, lda, tr, kmaj ? k : m, kmaj ? m : k, d, ds2, pl.ld_a, ds->sms, st)) != cudaSuccess)
-            return fail_cuda(e, "operand preparation (A)");
-        a_big = d;
-        a_small = ds2;
+    if (a_given) {
+        a_big = pre->big;
+        a_small = pre->small;
+    } else if (a_prep > 0) {
+        PreparedA pa;
+        if ((rc = prepare_a(pl, transa, m, k, A, lda, cursor, ds->sms, st, &pa))) return rc;
+        cursor += a_prep;
+        a_big = pa.big;
+        a_small = pa.small;
     }
     const float* b_big = B;
     const float* b_small = nullptr;
@@ -586,9 +621,11 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
 
 // ---- the host-array entry: internal copy streams ------------------------------------------
 
-// Two non-blocking streams per device for sgemm_host's copies in and out, with a
-// pool of events that order them against the caller's stream.  One mutex per
-// device serialises sgemm_host calls that use them (each call is synchronous).
+// Two non-blocking streams per (device, caller stream) for the host-array calls'
+// copies in and out, with a pool of events that order them against the caller's
+// stream.  Calls on different caller streams get different pipes, so their
+// copies share the host link instead of queueing behind each other; the mutex
+// serialises the queueing of calls on the same caller stream.
 struct HostPipe {
     std::mutex mu;
     cudaStream_t in = nullptr, out = nullptr;
@@ -602,12 +639,14 @@ struct HostPipe {
         return events[i];
     }
 };
-HostPipe g_pipe[kMaxDevices];
+std::map<std::pair<int, cudaStream_t>, std::unique_ptr<HostPipe>> g_pipes;  // never shrinks
 std::mutex g_pipe_init_mu;
 
-int host_pipe(int dev, HostPipe** out) {
+int host_pipe(int dev, cudaStream_t caller, HostPipe** out) {
     std::lock_guard<std::mutex> lk(g_pipe_init_mu);
-    HostPipe& hp = g_pipe[dev];
+    std::unique_ptr<HostPipe>& slot = g_pipes[std::make_pair(dev, caller)];
+    if (!slot) slot.reset(new HostPipe());
+    HostPipe& hp = *slot;
     cudaError_t e;
     if (!hp.in && (e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess)
         return fail_cuda(e, "cudaStreamCreateWithFlags");
@@ -615,7 +654,7 @@ int host_pipe(int dev, HostPipe** out) {
         return fail_cuda(e, "cudaStreamCreateWithFlags");
     {
         std::lock_guard<std::mutex> lk2(hp.mu);
-        for (size_t i = 0; i < 18; ++i)
+        for (size_t i = 0; i < 19; ++i)
             if (!hp.ev(i)) return fail(SGEMM_ERR_CUDA, "cudaEventCreateWithFlags failed");
     }
     *out = &hp;
@@ -637,9 +676,16 @@ PG_EXPORT int sgemm(char transa, char transb, int64_t m, int64_t n, int64_t k, f
                static_cast<cudaStream_t>(stream));
 }
 
-PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
-                         int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
-                         void* stream) {
+namespace pg {
+namespace {
+
+// The host-array call: queue the copies in, the product and the copies out on
+// `stream` (and the device's internal copy streams), then, when `wait`, wait for
+// all of it.  Without `wait`, `stream` is left ordered after the last copy out,
+// so synchronising it -- or the next call on it, whose copies reuse the staging
+// buffers -- waits for every copy of this call.
+int host_call(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
+              const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode, void* stream, bool wait) {
     int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
     if (rc) return rc;
     if (m == 0 || n == 0) return 0;
@@ -654,21 +700,39 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
     const size_t a_bytes = reads_ab ? region(lda_d * ca) : 0;
     const size_t b_bytes = reads_ab ? region(ldb_d * cb) : 0;
     const size_t c_bytes = region(ldc_d * n);
+
+    // Column slabs of C: A is copied in (and, if its kernel wants it transposed or
+    // split, prepared) once; each slab's columns of B (and of C when beta != 0)
+    // are copied in on one internal stream, the slab is computed on `stream`, and
+    // its result is copied out on a second internal stream, so the copies of one
+    // slab overlap the arithmetic of its neighbours.  Slabs stay at least 2048
+    // columns wide so each product still fills the GPU.  (Fewer, wider slabs sized
+    // to whole waves of the kernel measured slower end to end: the host link, not
+    // the arithmetic, bounds the tensor-core modes, and it is best kept busy by
+    // fine slabs.)
+#ifndef PG_HOST_SLAB_COLS
+#define PG_HOST_SLAB_COLS 2048  // compile-time tunable: narrowest slab
+#endif
+    const int64_t slab_min = PG_HOST_SLAB_COLS;
+    const int slabs = (reads_ab && is_notrans(transb) && n >= 2 * slab_min)
+                          ? static_cast<int>(std::min<int64_t>(8, n / slab_min))
+                          : 1;
+    sgemm_plan_t full{};
+    size_t pre_bytes = 0;
+    if (slabs > 1) {
+        // staging buffers are 256-byte aligned with ld multiples of 4: plan with them
+        const void* aligned = reinterpret_cast<const void*>(uintptr_t(256));
+        make_plan(transa, transb, m, n, k, alpha, aligned, lda_d, aligned, ldb_d, beta, mode, ds->sms, &full);
+        pre_bytes = prep_a_bytes(full, transa, m, k);
+    }
     void* stage = nullptr;
-    if ((rc = get_buffer(dev, st, kPurposeStaging, a_bytes + b_bytes + c_bytes, &stage))) return rc;
+    if ((rc = get_buffer(dev, st, kPurposeStaging, a_bytes + b_bytes + c_bytes + pre_bytes, &stage))) return rc;
     float* dA = reinterpret_cast<float*>(static_cast<char*>(stage));
     float* dB = reinterpret_cast<float*>(static_cast<char*>(stage) + a_bytes);
     float* dC = reinterpret_cast<float*>(static_cast<char*>(stage) + a_bytes + b_bytes);
-
-    // Column slabs of C: A is copied in once; each slab's columns of B (and of C
-    // when beta != 0) are copied in on one internal stream, the slab is computed
-    // on `stream`, and its result is copied out on a second internal stream, so
-    // the copies of one slab overlap the arithmetic of its neighbours.  Slabs
-    // stay at least 2048 columns wide so each product still fills the GPU.
-    const int slabs = (reads_ab && is_notrans(transb) && n >= 4096) ? static_cast<int>(std::min<int64_t>(8, n / 2048))
-                                                                      : 1;
+    char* dPre = static_cast<char*>(stage) + a_bytes + b_bytes + c_bytes;
     HostPipe* hp = nullptr;
-    if (slabs > 1 && (rc = host_pipe(dev, &hp))) return rc;
+    if (slabs > 1 && (rc = host_pipe(dev, st, &hp))) return rc;
     std::unique_lock<std::mutex> lk;
     if (hp) lk = std::unique_lock<std::mutex>(hp->mu);
     cudaStream_t s_in = hp ? hp->in : st;
@@ -691,6 +755,11 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
             note(cudaStreamWaitEvent(st, hp->ev(1), 0), "cudaStreamWaitEvent");
         }
     }
+    PreparedA pre;
+    if (rc == 0 && pre_bytes > 0) {
+        rc = prepare_a(full, transa, m, k, dA, lda_d, dPre, ds->sms, st, &pre);
+        if (rc == 0) g_launches += 1;
+    }
     for (int sl = 0; sl < slabs && rc == 0; ++sl) {
         const int64_t j0 = n * sl / slabs, j1 = n * (sl + 1) / slabs, w = j1 - j0;
         if (reads_ab) {
@@ -710,7 +779,8 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
         }
         if (rc == 0)
             rc = run(transa, transb, m, w, k, alpha, reads_ab ? dA : nullptr, reads_ab ? lda_d : 1,
-                     reads_ab ? dB + j0 * ldb_d : nullptr, reads_ab ? ldb_d : 1, beta, dC + j0 * ldc_d, ldc_d, mode, st);
+                     reads_ab ? dB + j0 * ldb_d : nullptr, reads_ab ? ldb_d : 1, beta, dC + j0 * ldc_d, ldc_d, mode, st,
+                     pre_bytes > 0 ? &pre : nullptr);
         if (rc == 0 && hp) {
             note(cudaEventRecord(hp->ev(3 + 2 * sl), st), "cudaEventRecord");
             note(cudaStreamWaitEvent(s_out, hp->ev(3 + 2 * sl), 0), "cudaStreamWaitEvent");
@@ -720,6 +790,16 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
                                    s_out),
                  "copy of C to the host");
     }
+    if (hp) {
+        // `stream` waits for everything queued on the internal streams (also after a
+        // failure: those copies touch the caller's arrays and the staging buffers).
+        for (cudaStream_t s : {s_in, s_out}) {
+            cudaEvent_t done = hp->ev(18);
+            if ((e = cudaEventRecord(done, s)) != cudaSuccess || (e = cudaStreamWaitEvent(st, done, 0)) != cudaSuccess)
+                if (rc == 0) rc = fail_cuda(e, "ordering the caller's stream after the copies");
+        }
+    }
+    if (!wait && rc == 0) return 0;
     // Every queued copy touches the caller's host arrays: wait for all of them
     // (also after a failure) before returning.
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess && rc == 0) rc = fail_cuda(e, "cudaStreamSynchronize");
@@ -728,6 +808,21 @@ PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t
         if ((e = cudaStreamSynchronize(s_out)) != cudaSuccess && rc == 0) rc = fail_cuda(e, "cudaStreamSynchronize");
     }
     return rc;
+}
+
+}  // namespace
+}  // namespace pg
+
+PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
+                         void* stream) {
+    return host_call(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode, stream, true);
+}
+
+PG_EXPORT int sgemm_host_async(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
+                               const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                               int64_t ldc, int mode, void* stream) {
+    return host_call(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode, stream, false);
 }
 
 PG_EXPORT int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,

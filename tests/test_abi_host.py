@@ -79,6 +79,16 @@ def test_invalid_arguments_rejected_before_device_work(lib, kw, code):
     assert "argument %d" % -code in pg.last_error()
 
 
+@pytest.mark.parametrize("entry", ["sgemm_host", "sgemm_host_async", "sgemm_noalloc"])
+@pytest.mark.parametrize("kw,code", [(dict(transa="X"), -1), (dict(m=-1), -3), (dict(lda=63), -8),
+                                     (dict(ldc=10), -13), (dict(mode=3), -14)])
+def test_other_entries_validate_like_sgemm(lib, entry, kw, code):
+    ta, tb, m, n, k, al, A, lda, B, ldb, be, C, ldc, mode = _with(**kw)
+    fn = getattr(lib, entry)
+    assert fn(ta.encode(), tb.encode(), m, n, k, al, A, lda, B, ldb, be, C, ldc, mode, None) == code
+    assert "argument %d" % -code in pg.last_error()
+
+
 def test_argument_order_is_signature_order(lib):
     # both transa and m are bad: the first in signature order is reported
     assert _call(lib, _with(transa="Z", m=-1)) == -1

@@ -273,12 +273,17 @@ def test_host_buffers_match_device_path(mode):
 def test_host_buffers_pipelined_slabs(mode):
     """n >= 4096: sgemm_host overlaps the copies of column slabs with the arithmetic
     of their neighbours (internal copy streams); the result must still match the
-    oracle, and the ld gap of the host C must stay untouched."""
-    p = synth.Problem(1000, 4100, 300, lda=1003, ldb=301, ldc=1005, alpha=1.25, beta=0.5, dist="normal", seed=29)
+    oracle, and the ld gap of the host C must stay untouched.  Two slabs of 3000
+    columns here; A is prepared once for all slabs (3xTF32: one split of A, one
+    of each B slab)."""
+    p = synth.Problem(2304, 6000, 300, lda=2307, ldb=301, ldc=2309, alpha=1.25, beta=0.5, dist="normal", seed=29)
     A, B, C = synth.make(p)
     Ch = C.clone().pin_memory()
+    before = pg.launch_count()
     pg.sgemm_host("N", "N", p.m, p.n, p.k, p.alpha, A.pin_memory(), p.lda, B.pin_memory(), p.ldb, p.beta, Ch,
                   p.ldc, mode)
+    launched = pg.launch_count() - before
+    assert launched == {"ffma": 2, "tf32": 2, "3xtf32": 5}[mode], launched
     cref, den = H.reference_full(p, A, B, C)
     res = oracle.check(H.logical(p, Ch), cref, den, oracle.TOL[mode])
     assert res["ok"], res

@@ -2,7 +2,8 @@
 capturable once the stream's workspace has been sized by an ordinary call; a call
 that would have to grow the workspace during capture is refused with
 SGEMM_ERR_CAPTURE; concurrent calls on different streams use different
-workspaces and both stay correct."""
+workspaces and both stay correct; sgemm_host_async calls on several streams
+overlap and each equals the synchronous sgemm_host result bit for bit."""
 import pytest
 import torch
 
@@ -89,3 +90,31 @@ def test_two_streams_run_concurrently(mode):
     torch.cuda.synchronize()
     for p, (dA, dB, dC), (A, B, C) in zip((p1, p2), dev, data):
         _check(p, mode, A, B, C, dC.cpu())
+
+
+def _pinned_problem(p):
+    A, B, C = synth.make(p)
+    return A.pin_memory(), B.pin_memory(), C.pin_memory(), C
+
+
+@pytest.mark.parametrize("same_stream", [False, True])
+def test_host_async_calls_overlap_and_match_sync(same_stream):
+    # one pipelined (n >= 4096: internal copy streams) and two single-slab problems
+    probs = [(synth.Problem(1024, 4608, 640, alpha=1.0, beta=0.75, dist="normal", seed=61), "ffma"),
+             (synth.Problem(700, 900, 1000, alpha=-0.5, beta=0.0, dist="normal", seed=62), "tf32"),
+             (synth.Problem(2048, 4096, 256, alpha=1.5, beta=1.0, dist="normal", seed=63), "3xtf32")]
+    data = [(_pinned_problem(p), p, mode) for p, mode in probs]
+    streams = [torch.cuda.Stream()] * 3 if same_stream else [torch.cuda.Stream() for _ in probs]
+    outs = []
+    for ((A, B, Ch, C), p, mode), s in zip(data, streams):
+        out = Ch.clone().pin_memory()
+        pg.sgemm_host_async("N", "N", p.m, p.n, p.k, p.alpha, A, p.lda, B, p.ldb, p.beta, out, p.ldc, mode, s)
+        outs.append(out)
+    for s in streams:
+        s.synchronize()
+    for ((A, B, Ch, C), p, mode), out in zip(data, outs):
+        ref = Ch.clone().pin_memory()
+        pg.sgemm_host("N", "N", p.m, p.n, p.k, p.alpha, A, p.lda, B, p.ldb, p.beta, ref, p.ldc, mode)
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), (p, mode)
+        _check(p, mode, A, B, C, out)
+    assert pg.device_status() == 0
