@@ -78,7 +78,7 @@ extern "C" {
 #define SGEMM_PREP_NONE 0      /* read in place through TMA                     */
 #define SGEMM_PREP_COPY 1      /* copied into the workspace with an aligned ld  */
 #define SGEMM_PREP_TRANSPOSE 2 /* copied transposed (trans = 'T')               */
-#define SGEMM_PREP_SPLIT 3     /* split into big/small TF32 parts (3xTF32)      */
+#define SGEMM_PREP_SPLIT 3     /* split into big/small TF32 parts (3xTF32 on SM pairs) */
 
 /*
  * sgemm -- C = alpha*op(A)*op(B) + beta*C on device memory.

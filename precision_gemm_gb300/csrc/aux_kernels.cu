@@ -13,28 +13,10 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"  // split_tf32
 
 namespace pg {
 namespace {
-
-// x = big + small with big holding x's leading 11 significant bits (the TF32
-// format: 8-bit exponent, 10 stored mantissa bits), rounded to nearest with
-// ties away from zero by adding half a TF32 unit to the magnitude bits before
-// clearing the low 13 bits.  small = x - big is exact in FP32 (|small| is at
-// most half a TF32 unit of x).  Non-finite inputs pass through as big with a
-// zero remainder; a finite value whose rounding would overflow is truncated.
-__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
-    const uint32_t u = __float_as_uint(x);
-    if (!isfinite(x)) {
-        big = x;
-        small = 0.0f;
-        return;
-    }
-    float b = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
-    if (!isfinite(b)) b = __uint_as_float(u & 0xFFFFE000u);
-    big = b;
-    small = x - b;
-}
 
 // Column sweep over a column-major rows x cols matrix: a CTA of 256 threads
 // covers TX = 2^tx_shift consecutive rows (32 <= TX <= 256, the smallest power of

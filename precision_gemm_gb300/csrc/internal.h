@@ -49,13 +49,15 @@ size_t ffma_smem_bytes(int bn);
 cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
                         int bn, dim3 grid, cudaStream_t stream);
 
-// tcgen05 kernel: tile 128 x bn, bn in {64, 128, 256}; split3 selects 3xTF32.
+// tcgen05 kernel: tile 128 x bn, bn in {64, 128, 256}; split3 selects 3xTF32,
+// whose TF32 split this kernel does itself in shared memory (it serves the
+// narrow shapes, m <= 128 or n <= 64, where a split pre-pass would cost more
+// HBM traffic than the product).
 int tc_bk(bool split3);
 int tc_stages(int bn, bool split3);
-int tc_threads();
+int tc_threads(bool split3);
 size_t tc_smem_bytes(int bn, bool split3);
-cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
-                      const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3,
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, bool split3,
                       dim3 grid, cudaStream_t stream);
 
 // tcgen05 kernel on SM pairs (cta_group::2, persistent, double-buffered TMEM):
@@ -71,7 +73,7 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CU
 // Operand preparation: dst(r, c) = src(r, c) (or src(c, r) when transposed) for
 // r < rows, c < cols, dst with leading dimension ldd.  With dst_small != null
 // the value is split into a TF32 "big" part (dst) and the exact remainder
-// (dst_small).
+// (dst_small), the operands of the SM-pair kernel's 3xTF32 mode.
 cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t rows,
                         int64_t cols, float* dst, float* dst_small, int64_t ldd,
                         int num_sms, cudaStream_t stream);

@@ -49,30 +49,43 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for phases completed by arrivals from other
+// CTAs of the cluster whose shared-memory writes the waiter must then see.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete, for at most
 // `timeout_ns`.  Returns false when the limit passes, or (when abort_flag is
 // non-null) as soon as another thread of the CTA has raised the abort flag.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                                   const volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (global_timer_ns() - t0 > timeout_ns) return false;
     }
@@ -83,6 +96,54 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* statu
     *abort_flag = 1;
     __threadfence_block();
     atomicCAS(status, 0, kStatusTimeout);
+}
+
+// ---- 3xTF32 split ------------------------------------------------------------------
+
+// x = big + small with big holding x's leading 11 significant bits (the TF32
+// format: 8-bit exponent, 10 stored mantissa bits), rounded to nearest with
+// ties away from zero by adding half a TF32 unit to the magnitude bits before
+// clearing the low 13 bits.  small = x - big is exact in FP32 (|small| is at
+// most half a TF32 unit of x).  Non-finite inputs pass through as big with a
+// zero remainder; a finite value whose rounding would overflow is truncated.
+__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
+    const uint32_t u = __float_as_uint(x);
+    if (!isfinite(x)) {
+        big = x;
+        small = 0.0f;
+        return;
+    }
+    float b = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
+    if (!isfinite(b)) b = __uint_as_float(u & 0xFFFFE000u);
+    big = b;
+    small = x - b;
+}
+
+// Split the BYTES of FP32 values at `tile` (shared memory, TMA-written) in
+// place: each value becomes its TF32 big part and its remainder goes to the same
+// offset at tile + small_offset.  A swizzled layout is a function of the byte
+// address inside 1 KiB-aligned atoms, so with both regions 1 KiB aligned the
+// remainder tile has the layout of the big one.  Thread t of NTHREADS takes the
+// 16-byte chunks t, t + NTHREADS, ... (a warp covers 512 contiguous bytes) and
+// loads all of its chunks before it stores any: a load that might alias an
+// earlier store of the same thread would otherwise wait for it.
+template <int BYTES, int NTHREADS>
+__device__ __forceinline__ void split_tile_in_place(uint8_t* tile, int small_offset, int t) {
+    static_assert(BYTES % (16 * NTHREADS) == 0, "whole chunks per thread");
+    constexpr int CH = BYTES / (16 * NTHREADS);
+    float4 v[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) v[c] = *reinterpret_cast<const float4*>(tile + 16 * (t + c * NTHREADS));
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        float4 sm;
+        split_tf32(v[c].x, v[c].x, sm.x);
+        split_tf32(v[c].y, v[c].y, sm.y);
+        split_tf32(v[c].z, v[c].z, sm.z);
+        split_tf32(v[c].w, v[c].w, sm.w);
+        *reinterpret_cast<float4*>(tile + 16 * (t + c * NTHREADS)) = v[c];
+        *reinterpret_cast<float4*>(tile + small_offset + 16 * (t + c * NTHREADS)) = sm;
+    }
 }
 
 // ---- TMA -----------------------------------------------------------------------

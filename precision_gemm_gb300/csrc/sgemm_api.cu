@@ -122,14 +122,27 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     const bool tc = mode != SGEMM_FFMA;
     const bool split3 = mode == SGEMM_3XTF32;
 
+    // Tile width: 64 for n <= 64; otherwise 128 for the FFMA kernel (two CTAs per
+    // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05.
+    int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
+    const int fbn = g_force_bn.load();
+    if (fbn) bn = fbn;
+    pl->bn = bn;
+    // Tensor-core modes run on SM pairs (256-row tiles, cta_group::2) when m > 128;
+    // a single-SM 128-row tile serves m <= 128 and the 64-wide tile.
+    const bool pair = tc && m > kBM && bn >= 128;
+
     // Operand preparation: TMA needs a 16-byte aligned base and a leading
     // dimension that is a multiple of 16 bytes.  The tensor-core kernels read
     // either orientation of A and B (K-major or M/N-major descriptors), so their
     // copies and 3xTF32 splits keep the stored orientation; the FFMA kernel reads
     // A M-major and B K-major only, so a transposed operand is copied transposed.
+    // 3xTF32 on SM pairs reads operands split by a pre-pass (the large shapes, where
+    // the pre-pass is cheap next to the product); the single-SM kernel splits them
+    // itself in shared memory (the narrow shapes, where a pre-pass would dominate).
     const bool a_ok = aligned16(A) && (lda % 4 == 0);
     const bool b_ok = aligned16(B) && (ldb % 4 == 0);
-    if (split3) {
+    if (split3 && pair) {
         pl->prep_a = SGEMM_PREP_SPLIT;
         pl->prep_b = SGEMM_PREP_SPLIT;
     } else if (tc) {
@@ -147,20 +160,11 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->ld_a = pl->prep_a == SGEMM_PREP_NONE ? lda : round_up(rows_a, 4);
     pl->ld_b = pl->prep_b == SGEMM_PREP_NONE ? ldb : round_up(rows_b, 4);
 
-    // Tile width: 64 for n <= 64; otherwise 128 for the FFMA kernel (two CTAs per
-    // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05.
-    int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
-    const int fbn = g_force_bn.load();
-    if (fbn) bn = fbn;
-    pl->bn = bn;
-    // Tensor-core modes run on SM pairs (256-row tiles, cta_group::2) when m > 128;
-    // a single-SM 128-row tile serves m <= 128 and the 64-wide tile.
-    const bool pair = tc && m > kBM && bn >= 128;
     pl->kernel = !tc ? SGEMM_KERNEL_FFMA : (pair ? SGEMM_KERNEL_TC2 : SGEMM_KERNEL_TC);
     pl->bm = pair ? 2 * kBM : kBM;
     pl->bk = !tc ? kFfmaBK : (pair ? tc2_bk(split3) : tc_bk(split3));
     pl->stages = !tc ? ffma_stages(bn) : (pair ? tc2_stages(bn, split3) : tc_stages(bn, split3));
-    pl->threads = !tc ? ffma_threads(bn) : (pair ? tc2_threads() : tc_threads());
+    pl->threads = !tc ? ffma_threads(bn) : (pair ? tc2_threads() : tc_threads(split3));
     pl->ctas_per_sm = tc ? 1 : ffma_ctas_per_sm(bn);
     pl->smem_bytes = !tc ? ffma_smem_bytes(bn) : (pair ? tc2_smem_bytes(bn, split3) : tc_smem_bytes(bn, split3));
     pl->tiles_m = static_cast<int>(cdiv(m, pl->bm));
@@ -187,7 +191,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->k_blocks_per_split = static_cast<int>(per);
 
     size_t ws = 0;
-    const int parts = split3 ? 2 : 1;
+    const int parts = (split3 && pair) ? 2 : 1;
     if (pl->prep_a != SGEMM_PREP_NONE) ws += parts * region(pl->ld_a * (rows_a == m ? k : m));
     if (pl->prep_b != SGEMM_PREP_NONE) ws += parts * region(pl->ld_b * (rows_b == k ? n : k));
     if (split > 1) ws += region(split * round_up(m, 4) * n);
@@ -349,7 +353,7 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
                 GemmParams& gp, int num_sms, cudaStream_t st) {
     int rc;
     cudaError_t e;
-    CUtensorMap tmA, tmB, tmAs, tmBs;
+    CUtensorMap tmA, tmB;
     if (pl.kernel == SGEMM_KERNEL_FFMA) {
         const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
         if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
@@ -381,20 +385,20 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
         };
         if ((rc = encode_a(&tmA, a_big))) return rc;
         if ((rc = encode_b(&tmB, b_big))) return rc;
-        tmAs = tmA;
-        tmBs = tmB;
-        if (split3) {
-            if ((rc = encode_a(&tmAs, a_small))) return rc;
-            if ((rc = encode_b(&tmBs, b_small))) return rc;
-        }
         if (pair) {
+            // 3xTF32 on SM pairs reads the pre-split parts: big through tmA/tmB, small through tmAs/tmBs
+            CUtensorMap tmAs = tmA, tmBs = tmB;
+            if (split3) {
+                if ((rc = encode_a(&tmAs, a_small))) return rc;
+                if ((rc = encode_b(&tmBs, b_small))) return rc;
+            }
             int pairs = 0;
             const int units = pl.tiles_m * pl.tiles_n * pl.split_k;
             if ((e = launch_tc2(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, units, num_sms, st, &pairs)) != cudaSuccess)
                 return fail_cuda(e, "tcgen05 SM-pair GEMM kernel");
         } else {
             const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
-            if ((e = launch_tc(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
+            if ((e = launch_tc(tmA, tmB, gp, pl.bn, split3, grid, st)) != cudaSuccess)
                 return fail_cuda(e, "tcgen05 GEMM kernel");
         }
     }
@@ -412,13 +416,13 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
 // sgemm_host does for its column slabs).
 struct PreparedA {
     const float* big = nullptr;
-    const float* small = nullptr;  // 3xTF32 remainder part
+    const float* small = nullptr;  // 3xTF32 remainder part (split pre-pass)
 };
 
 // Device bytes of A's preparation under plan pl (0 when A is read in place).
 size_t prep_a_bytes(const sgemm_plan_t& pl, char transa, int64_t m, int64_t k) {
     if (pl.prep_a == SGEMM_PREP_NONE) return 0;
-    const int parts = pl.mode == SGEMM_3XTF32 ? 2 : 1;
+    const int parts = pl.prep_a == SGEMM_PREP_SPLIT ? 2 : 1;
     const int64_t cols_a = (pl.kernel != SGEMM_KERNEL_FFMA && !is_notrans(transa)) ? m : k;
     return parts * region(pl.ld_a * cols_a);
 }
@@ -426,9 +430,10 @@ size_t prep_a_bytes(const sgemm_plan_t& pl, char transa, int64_t m, int64_t k) {
 // Prepare A as plan pl asks into dst (prep_a_bytes(pl, ...) bytes); one launch.
 int prepare_a(const sgemm_plan_t& pl, char transa, int64_t m, int64_t k, const float* A, int64_t lda, char* dst,
               int num_sms, cudaStream_t st, PreparedA* out) {
-    const int parts = pl.mode == SGEMM_3XTF32 ? 2 : 1;
     float* d = reinterpret_cast<float*>(dst);
-    float* ds2 = parts == 2 ? reinterpret_cast<float*>(dst + prep_a_bytes(pl, transa, m, k) / 2) : nullptr;
+    float* ds2 = pl.prep_a == SGEMM_PREP_SPLIT
+                     ? reinterpret_cast<float*>(dst + prep_a_bytes(pl, transa, m, k) / 2)
+                     : nullptr;
     const bool tr = pl.prep_a == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into M-major
     const bool kmaj = !tr && !is_notrans(transa);      // tensor cores: stored k x m, kept as is
     cudaError_t e = launch_prep(A, lda, tr, kmaj ? k : m, kmaj ? m : k, d, ds2, pl.ld_a, num_sms, st);
@@ -465,7 +470,6 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     void* ws = nullptr;
     if ((rc = get_buffer(dev, st, kPurposeWorkspace, pl.workspace_bytes, &ws))) return rc;
     const bool split3 = mode == SGEMM_3XTF32;
-    const int parts = split3 ? 2 : 1;
     char* cursor = static_cast<char*>(ws);
 
     const float* a_big = A;
@@ -487,7 +491,7 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
         const int64_t cols_b = (pl.kernel != SGEMM_KERNEL_FFMA && !is_notrans(transb)) ? k : n;
         cursor += region(pl.ld_b * cols_b);
         float* ds2 = nullptr;
-        if (parts == 2) {
+        if (pl.prep_b == SGEMM_PREP_SPLIT) {
             ds2 = reinterpret_cast<float*>(cursor);
             cursor += region(pl.ld_b * cols_b);
         }
@@ -616,7 +620,7 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     gp.timeout_ns = g_timeout_ns.load();
     gp.status = ds->status;
 
-    return launch_gemm(pl, false, false, false, A, A, B, B, m, n, k, gp, ds->sms, st);
+    return launch_gemm(pl, false, false, false, A, nullptr, B, nullptr, m, n, k, gp, ds->sms, st);
 }
 
 // ---- the host-array entry: internal copy streams ------------------------------------------

@@ -10,10 +10,11 @@
 // thread replaces per-warp MMA fragments, so the pages' per-warp "shift"
 // barriers have nothing left to order.
 //
-// Warp roles (192 threads):
+// Warp roles (192 threads; 320 in 3xTF32):
 //   warp 0      TMA loader (one thread): A as four 32-row boxes, B as one box
 //   warp 1      allocates TMEM; one thread issues the MMAs; frees TMEM at exit
 //   warps 2-5   epilogue; warp w may access TMEM lanes 32*(w%4) .. +31
+//   warps 6-9   3xTF32 only: split each landed slot into TF32 parts
 //
 // Shared-memory operand layouts (canonical tcgen05 layouts, 1 KiB aligned):
 //   A (column-major, M-major): per 32-row group of M a box of BK rows of k,
@@ -28,11 +29,15 @@
 //     rows with the 64-byte swizzle (groups of 512 B).  The k-step kk starts at
 //     +32*kk bytes inside the swizzle atom.
 //
-// 3xTF32 (SPLIT3): each operand arrives as a "big" TF32 part and the exact
-// remainder ("small"), prepared by the split pre-pass; per k-step the thread
-// issues small*big, big*small, big*big into the same accumulator (the
+// 3xTF32 (SPLIT3): TMA brings the FP32 tiles of A and B into the "big" halves
+// of the slot; four transform warps then split every value in place into its
+// TF32 "big" part and write the exact remainder ("small") at the same offset of
+// the slot's other half, fence the generic-proxy writes for the tensor core and
+// arrive on the slot's "ready" barrier, which the MMA thread waits for.  Per
+// k-step it issues small*big, big*small, big*big into the same accumulator (the
 // small*small term is below FP32 resolution and dropped).  Four operand tiles
-// per slot halve BK to 16 so four slots still fit.
+// per slot halve BK to 16 so four slots still fit; only half of each slot comes
+// from memory, so 3xTF32 reads each operand byte from DRAM once, like TF32.
 //
 // Every wait is bounded; on expiry the CTA records the status, lets its
 // in-flight TMA copies and MMAs finish (bounded), frees TMEM and exits.
@@ -54,10 +59,12 @@ struct TcCfg {
     static constexpr int B_BYTES = BN * BK * 4;  // one part of B
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
     static constexpr int STAGE_BYTES = OPS * (A_BYTES + B_BYTES);
+    static constexpr int TMA_BYTES = A_BYTES + B_BYTES;  // FP32 tiles loaded per slot
     static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-    static constexpr int THREADS = 192;
-    static constexpr int BAR_BYTES = (2 * STAGES + 1) * 8 + 16;
+    static constexpr int XF_WARPS = SPLIT3 ? 4 : 0;      // transform warps
+    static constexpr int THREADS = 192 + 32 * XF_WARPS;
+    static constexpr int BAR_BYTES = (3 * STAGES + 1) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = BN;  // power of two >= 32
     static_assert(STAGES >= 2, "ring too shallow");
@@ -66,20 +73,21 @@ struct TcCfg {
 };
 
 template <int BN, bool SPLIT3>
-__global__ void __launch_bounds__(192, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
-                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
+__global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
     using Cfg = TcCfg<BN, SPLIT3>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
+    // [0,S) full, [S,2S) empty, 2S accum, [2S+1, 3S+1) ready (3xTF32)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + S);
     const uint32_t accum_bar = smem_u32(bars + 2 * S);
+    const uint32_t ready0 = smem_u32(bars + 2 * S + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -96,6 +104,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
+            if (SPLIT3) mbar_init(ready0 + 8 * s, Cfg::XF_WARPS);
         }
         mbar_init(accum_bar, 1);
         *abort_flag = 0;
@@ -115,10 +124,6 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
-            if (SPLIT3) {
-                prefetch_tmap(&tmAs);
-                prefetch_tmap(&tmBs);
-            }
             int issued = 0;
             if (!(p.debug_flags & 1)) {
                 for (int it = 0; it < nkb; ++it) {
@@ -128,11 +133,9 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     const uint32_t full = full0 + 8 * s;
-                    mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+                    mbar_arrive_expect_tx(full, Cfg::TMA_BYTES);
                     const int32_t kc = (kb0 + it) * Cfg::BK;
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
-                    // A: one 3-D box {32 rows, BK, 4 row groups} when m % 32 == 0, else four
-                    // 2-D boxes of 32 rows (both land as 4 x [BK][32] row groups).
                     // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
                     // box {32 rows, BK, 4 row groups} when m % 32 == 0, else four 2-D boxes
                     // of 32 rows (both land as 4 x [BK][32] row groups).
@@ -162,14 +165,9 @@ __global__ void __launch_bounds__(192, 1)
                                             full);
                         }
                     };
+                    // FP32 tiles into the big halves: [A big][A small][B big][B small]
                     load_a(slot, &tmA);
-                    uint32_t b_slot = slot + Cfg::A_BYTES;
-                    if (SPLIT3) {
-                        load_a(slot + Cfg::A_BYTES, &tmAs);
-                        b_slot = slot + 2 * Cfg::A_BYTES;
-                        load_b(b_slot + Cfg::B_BYTES, &tmBs);
-                    }
-                    load_b(b_slot, &tmB);
+                    load_b(slot + Cfg::OPS * Cfg::A_BYTES, &tmB);
                     issued = it + 1;
                 }
             }
@@ -184,7 +182,8 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
-                if (!mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
+                // 3xTF32: the transform warps have split the slot
+                if (!mbar_wait_bounded((SPLIT3 ? ready0 : full0) + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
                     raise_abort(abort_flag, p.status);
                     break;
                 }
@@ -215,6 +214,26 @@ __global__ void __launch_bounds__(192, 1)
             mma_commit(accum_bar);  // accumulator complete (also after an abort)
         }
         __syncwarp();
+    } else if (warp >= 6) {
+        // ---------------- 3xTF32 transform (warps 6..9) ----------------
+        if constexpr (SPLIT3) {
+            const int t = threadIdx.x - 192;
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % S;
+                const bool landed = __all_sync(
+                    0xffffffffu, mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag));
+                if (!landed) {
+                    if (lane == 0) raise_abort(abort_flag, p.status);
+                    break;
+                }
+                uint8_t* slot = smem + s * Cfg::STAGE_BYTES;
+                split_tile_in_place<Cfg::A_BYTES, 32 * Cfg::XF_WARPS>(slot, Cfg::A_BYTES, t);
+                split_tile_in_place<Cfg::B_BYTES, 32 * Cfg::XF_WARPS>(slot + 2 * Cfg::A_BYTES, Cfg::B_BYTES, t);
+                fence_proxy_async_smem();  // the tensor core reads these writes
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ready0 + 8 * s);
+            }
+        }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;
@@ -279,24 +298,24 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int BN, bool SPLIT3>
-cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
-                        const CUtensorMap& tmBs, const GemmParams& p, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, dim3 grid,
+                        cudaStream_t stream) {
     using Cfg = TcCfg<BN, SPLIT3>;
     auto kern = tc_gemm_kernel<BN, SPLIT3>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmAs, tmB, tmBs, p);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 
 template <bool SPLIT3>
-cudaError_t launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b,
-                      const CUtensorMap& bs, const GemmParams& p, dim3 grid, cudaStream_t st) {
+cudaError_t launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, dim3 grid,
+                      cudaStream_t st) {
     switch (bn) {
-        case 64: return launch_impl<64, SPLIT3>(a, as, b, bs, p, grid, st);
-        case 128: return launch_impl<128, SPLIT3>(a, as, b, bs, p, grid, st);
-        case 256: return launch_impl<256, SPLIT3>(a, as, b, bs, p, grid, st);
+        case 64: return launch_impl<64, SPLIT3>(a, b, p, grid, st);
+        case 128: return launch_impl<128, SPLIT3>(a, b, p, grid, st);
+        case 256: return launch_impl<256, SPLIT3>(a, b, p, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -316,14 +335,12 @@ constexpr size_t smem_of(int bn) {
 
 int tc_bk(bool split3) { return split3 ? TcCfg<256, true>::BK : TcCfg<256, false>::BK; }
 int tc_stages(int bn, bool split3) { return split3 ? stages_of<true>(bn) : stages_of<false>(bn); }
-int tc_threads() { return 192; }
+int tc_threads(bool split3) { return split3 ? TcCfg<256, true>::THREADS : TcCfg<256, false>::THREADS; }
 size_t tc_smem_bytes(int bn, bool split3) { return split3 ? smem_of<true>(bn) : smem_of<false>(bn); }
 
-cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,
-                      const CUtensorMap& tmBs, const GemmParams& p, int bn, bool split3, dim3 grid,
-                      cudaStream_t stream) {
-    return split3 ? launch_bn<true>(bn, tmA, tmAs, tmB, tmBs, p, grid, stream)
-                  : launch_bn<false>(bn, tmA, tmAs, tmB, tmBs, p, grid, stream);
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, bool split3,
+                      dim3 grid, cudaStream_t stream) {
+    return split3 ? launch_bn<true>(bn, tmA, tmB, p, grid, stream) : launch_bn<false>(bn, tmA, tmB, p, grid, stream);
 }
 
 }  // namespace pg

@@ -127,8 +127,16 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
         assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc2")
         assert p["ctas_per_sm"] == (2 if mode == "ffma" else 1)
     assert plan(8192, 8192, 8192, "ffma")["prep_a_name"] == "none"
-    assert plan(8192, 8192, 8192, "3xtf32")["prep_a_name"] == "split"
-    assert plan(8192, 8192, 8192, "3xtf32")["launches"] == 3
+    # 3xTF32 on SM pairs: a split pre-pass per operand, then the GEMM
+    x = plan(8192, 8192, 8192, "3xtf32")
+    assert x["prep_a_name"] == "split" and x["prep_b_name"] == "split" and x["launches"] == 3
+    assert x["workspace_bytes"] == 4 * 8192 * 8192 * 4
+    # narrow shapes (single-SM kernel): the kernel splits the operands itself in shared
+    # memory with four extra warps; no pre-pass, no operand workspace
+    t = plan(8192, 64, 8192, "3xtf32")
+    assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
+    assert t["threads"] == plan(8192, 64, 8192, "tf32")["threads"] + 128
+    assert t["launches"] == 1 + (t["split_k"] > 1)
 
 
 def test_plan_skinny_k_uses_deterministic_split(lib):
@@ -167,9 +175,14 @@ def test_plan_transposed_operands(lib):
     t = plan(300, 200, 100, "tf32", transa="T", transb="T", lda=104, ldb=204)
     assert t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
     assert t["ld_a"] == 104 and t["ld_b"] == 204 and t["launches"] == 1
-    # 3xTF32 splits them without transposing: ld is the stored row count rounded to 4
+    # 3xTF32 on SM pairs splits them without transposing: ld is the stored row count rounded to 4
     x = plan(300, 200, 101, "3xtf32", transa="T", transb="T")
     assert x["prep_a_name"] == "split" and x["ld_a"] == 104 and x["ld_b"] == 200
+    # the single-SM kernel reads them in place and splits in shared memory; a stored
+    # row count that is not a multiple of 4 still needs a plain copy, ld rounded up
+    y = plan(100, 64, 101, "3xtf32", transa="T", transb="T")
+    assert y["kernel_name"] == "tc" and y["prep_a_name"] == "copy" and y["ld_a"] == 104
+    assert y["prep_b_name"] == "none" and y["ld_b"] == 64
     # a misaligned transposed operand is copied (not transposed) for the tensor cores
     c = plan(300, 200, 100, "tf32", transa="T", lda=101)
     assert c["prep_a_name"] == "copy" and c["ld_a"] == 100

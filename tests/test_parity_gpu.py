@@ -274,8 +274,8 @@ def test_host_buffers_pipelined_slabs(mode):
     """n >= 4096: sgemm_host overlaps the copies of column slabs with the arithmetic
     of their neighbours (internal copy streams); the result must still match the
     oracle, and the ld gap of the host C must stay untouched.  Two slabs of 3000
-    columns here; A is prepared once for all slabs (3xTF32: one split of A, one
-    of each B slab)."""
+    columns here; A is prepared once for all slabs (3xTF32 on SM pairs: one split
+    of A, then one split of each B slab and the slab's product)."""
     p = synth.Problem(2304, 6000, 300, lda=2307, ldb=301, ldc=2309, alpha=1.25, beta=0.5, dist="normal", seed=29)
     A, B, C = synth.make(p)
     Ch = C.clone().pin_memory()
