@@ -190,6 +190,8 @@ typedef struct sgemm_plan {
     size_t smem_bytes;       /* dynamic shared memory of the GEMM kernel        */
     size_t workspace_bytes;  /* device workspace the call needs                 */
     int launches;            /* kernels the call launches                       */
+    int tail_tiles;          /* SM pairs: last-wave tiles whose K is split ...  */
+    int tail_split;          /* ... into this many slices (1: none)             */
 } sgemm_plan_t;
 
 /*

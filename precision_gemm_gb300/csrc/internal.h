@@ -32,6 +32,16 @@ struct GemmParams {
     int32_t a_kmajor;        // tcgen05 kernels: A is read K-major (transa = 'T'), else M-major
     int32_t b_mnmajor;       // tcgen05 kernels: B is read N-major (transb = 'T'), else K-major
     int32_t b3d;             // tcgen05 kernels, N-major B: tensor map 3-D {32, k, n/32}
+    // Last-wave split (SM-pair kernel, split == 1): tiles [tail_first, tiles) each
+    // run as tail_split K slices of tail_kb blocks; every slice stores its partial
+    // 256 x BN block in tail_P ([tail tile][slice][column][row]), and per epilogue
+    // warp region a counter in tail_cnt (zeroed before the launch) finds the last
+    // slice to finish, which sums the partials in slice order and writes C.
+    int32_t tail_first;
+    int32_t tail_split;      // 1: no tail split
+    int32_t tail_kb;
+    float* tail_P;
+    int* tail_cnt;
     uint64_t timeout_ns;     // limit of every bounded wait
     int* status;             // per-device status word
 };
@@ -64,6 +74,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 // pair tile 256 x bn, bn in {128, 256}; launches min(units, resident pairs) pairs.
 int tc2_bk(bool split3);
 int tc2_threads();
+int tc2_epilogue_warps();  // per CTA
 int tc2_stages(int bn, bool split3);
 size_t tc2_smem_bytes(int bn, bool split3);
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CUtensorMap& tmB,

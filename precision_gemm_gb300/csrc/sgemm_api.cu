@@ -103,12 +103,24 @@ int validate(char transa, char transb, int64_t m, int64_t n, int64_t k, float al
 
 size_t region(int64_t elems) { return static_cast<size_t>(round_up(elems * 4, 256)); }
 
-// The planner.  Pure host arithmetic: no device is touched.
+// Workspace of the last-wave split: the partial blocks, and one arrival counter
+// per (tail tile, epilogue warp region).
+size_t tail_bytes(const sgemm_plan_t& pl) {
+    return region(static_cast<int64_t>(pl.tail_tiles) * pl.tail_split * pl.bm * pl.bn);
+}
+size_t tail_counter_bytes(const sgemm_plan_t& pl) {
+    return region(static_cast<int64_t>(pl.tail_tiles) * 2 * tc2_epilogue_warps());
+}
+
+// The planner.  Pure host arithmetic: no device is touched.  allow_tail = false
+// (the allocation-free entry) never plans a last-wave split.
 void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,
-               int64_t lda, const void* B, int64_t ldb, float beta, int mode, int num_sms, sgemm_plan_t* pl) {
+               int64_t lda, const void* B, int64_t ldb, float beta, int mode, int num_sms, sgemm_plan_t* pl,
+               bool allow_tail = true) {
     std::memset(pl, 0, sizeof *pl);
     pl->mode = mode;
     pl->split_k = 1;
+    pl->tail_split = 1;
     pl->bm = kBM;
     if (m == 0 || n == 0) {
         pl->kernel = SGEMM_KERNEL_NONE;
@@ -190,11 +202,26 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->split_k = static_cast<int>(split);
     pl->k_blocks_per_split = static_cast<int>(per);
 
+    // Last-wave split (SM pairs): when the tiles fill whole waves of pairs and a
+    // last wave at most half full, cut each last-wave tile's K into s slices (at
+    // least 8 K blocks each, s <= 4) so the last wave keeps every pair busy.
+    if (pair && split == 1 && g_force_split.load() == 0 && allow_tail) {
+        const int64_t waves = tiles / capacity, rem = tiles % capacity;
+        if (waves >= 1 && rem > 0 && 2 * rem <= capacity) {
+            const int64_t s = std::min<int64_t>({capacity / rem, 4, pl->k_blocks / 8});
+            if (s >= 2) {
+                pl->tail_tiles = static_cast<int>(rem);
+                pl->tail_split = static_cast<int>(s);
+            }
+        }
+    }
+
     size_t ws = 0;
     const int parts = (split3 && pair) ? 2 : 1;
     if (pl->prep_a != SGEMM_PREP_NONE) ws += parts * region(pl->ld_a * (rows_a == m ? k : m));
     if (pl->prep_b != SGEMM_PREP_NONE) ws += parts * region(pl->ld_b * (rows_b == k ? n : k));
     if (split > 1) ws += region(split * round_up(m, 4) * n);
+    if (pl->tail_split > 1) ws += tail_bytes(*pl) + tail_counter_bytes(*pl);
     pl->workspace_bytes = ws;
     pl->launches = (pl->prep_a != SGEMM_PREP_NONE) + (pl->prep_b != SGEMM_PREP_NONE) + 1 + (split > 1);
 }
@@ -393,7 +420,9 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
                 if ((rc = encode_b(&tmBs, b_small))) return rc;
             }
             int pairs = 0;
-            const int units = pl.tiles_m * pl.tiles_n * pl.split_k;
+            const int units = pl.tail_split > 1
+                                  ? pl.tiles_m * pl.tiles_n + pl.tail_tiles * (pl.tail_split - 1)
+                                  : pl.tiles_m * pl.tiles_n * pl.split_k;
             if ((e = launch_tc2(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, units, num_sms, st, &pairs)) != cudaSuccess)
                 return fail_cuda(e, "tcgen05 SM-pair GEMM kernel");
         } else {
@@ -516,11 +545,22 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
         gp.P = reinterpret_cast<float*>(cursor);
         gp.ldp = round_up(m, 4);
         gp.p_stride = gp.ldp * n;
+        cursor += region(pl.split_k * gp.ldp * n);
     }
     gp.tiles_m = pl.tiles_m;
     gp.tiles_n = pl.tiles_n;
     gp.kb_total = pl.k_blocks;
     gp.kb_per_split = pl.k_blocks_per_split;
+    gp.tail_split = pl.tail_split;
+    gp.tail_first = pl.tiles_m * pl.tiles_n - pl.tail_tiles;
+    if (pl.tail_split > 1) {
+        gp.tail_kb = static_cast<int32_t>(cdiv(pl.k_blocks, pl.tail_split));
+        gp.tail_P = reinterpret_cast<float*>(cursor);
+        cursor += tail_bytes(pl);
+        gp.tail_cnt = reinterpret_cast<int*>(cursor);
+        if ((e = cudaMemsetAsync(gp.tail_cnt, 0, tail_counter_bytes(pl), st)) != cudaSuccess)
+            return fail_cuda(e, "cudaMemsetAsync (last-wave counters)");
+    }
     gp.group_m = PG_GROUP_M;
     gp.c_vec = aligned16(C) && (ldc % 4 == 0);
     gp.debug_flags = g_debug.load();
@@ -578,7 +618,7 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     int rc = current_device(&dev, &ds);
     if (rc) return rc;
     sgemm_plan_t pl;
-    make_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, mode, ds->sms, &pl);
+    make_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, mode, ds->sms, &pl, false);
     cudaError_t e;
     if (pl.kernel == SGEMM_KERNEL_NONE) return 0;
     if (pl.kernel == SGEMM_KERNEL_SCALE) {

@@ -11,7 +11,11 @@
 //
 // The kernel is persistent: each pair walks work units (tile, K slice) with a
 // static stride, and the accumulator is double-buffered in TMEM (2 x BN columns)
-// so the epilogue of one unit overlaps the MMAs of the next.
+// so the epilogue of one unit overlaps the MMAs of the next.  When the tiles fill
+// whole waves of pairs plus a partial last wave, the last wave's tiles are cut
+// into K slices that occupy the otherwise idle pairs; each slice leaves a
+// partial block in global memory and the last slice of a region to finish adds
+// them in slice order (deterministic) and writes C.
 //
 // Warp roles, in both CTAs of the pair (320 threads each):
 //   warp 0      TMA loader: this CTA's A rows and B columns for every k-block,
@@ -168,7 +172,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
     const int pair = blockIdx.x >> 1;
     const int pairs = gridDim.x >> 1;
     const int tiles = p.tiles_m * p.tiles_n;
-    const int units = tiles * p.split;
+    const bool tail_on = p.tail_split > 1;
+    const int units = tail_on ? p.tail_first + (tiles - p.tail_first) * p.tail_split : tiles * p.split;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -195,16 +200,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
 
-    // Work unit -> (pair tile, K slice, k-block range).
-    auto unit_geometry = [&](int u, int64_t& m0, int64_t& n0, int& slice, int& kb0, int& nkb) {
-        const int t = u % tiles;
-        slice = u / tiles;
+    // Work unit -> (pair tile t, K slice, k-block range).
+    auto unit_geometry = [&](int u, int64_t& m0, int64_t& n0, int& slice, int& kb0, int& nkb, int& t) {
+        if (tail_on) {
+            if (u < p.tail_first) {
+                t = u;
+                slice = 0;
+                kb0 = 0;
+                nkb = p.kb_total;
+            } else {
+                const int v = u - p.tail_first;
+                t = p.tail_first + v / p.tail_split;
+                slice = v % p.tail_split;
+                kb0 = slice * p.tail_kb;
+                nkb = min(kb0 + p.tail_kb, p.kb_total) - kb0;
+            }
+        } else {
+            t = u % tiles;
+            slice = u / tiles;
+            kb0 = slice * p.kb_per_split;
+            nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
+        }
         int tm, tn;
         tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
         m0 = static_cast<int64_t>(tm) * (2 * Cfg::BM);
         n0 = static_cast<int64_t>(tn) * BN;
-        kb0 = slice * p.kb_per_split;
-        nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
     };
 
     if (warp == 0) {
@@ -221,8 +241,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
             bool ok = true;
             for (int u = pair; u < units && ok; u += pairs) {
                 int64_t m0, n0;
-                int slice, kb0, nkb;
-                unit_geometry(u, m0, n0, slice, kb0, nkb);
+                int slice, kb0, nkb, t;
+                unit_geometry(u, m0, n0, slice, kb0, nkb, t);
                 const int32_t ma = static_cast<int32_t>(m0 + Cfg::BM * rank);
                 const int32_t nb = static_cast<int32_t>(n0 + Cfg::BNH * rank);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -287,8 +307,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
             const uint32_t idesc = idesc_tf32(2 * Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
             for (int u = pair; u < units && ok; u += pairs, ++lu) {
                 int64_t m0, n0;
-                int slice, kb0, nkb;
-                unit_geometry(u, m0, n0, slice, kb0, nkb);
+                int slice, kb0, nkb, t;
+                unit_geometry(u, m0, n0, slice, kb0, nkb, t);
                 const int buf = lu & 1;
                 if (!mbar_wait_bounded(acc_empty0 + 8 * buf, ((lu >> 1) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                     raise_abort(abort_flag, p.status);
@@ -344,8 +364,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
         int lu = 0;
         for (int u = pair; u < units; u += pairs, ++lu) {
             int64_t m0, n0;
-            int slice, kb0, nkb;
-            unit_geometry(u, m0, n0, slice, kb0, nkb);
+            int slice, kb0, nkb, tile;
+            unit_geometry(u, m0, n0, slice, kb0, nkb, tile);
+            const bool tail = tail_on && tile >= p.tail_first;
+            const int64_t i_loc = Cfg::BM * rank + 32 * q + lane;  // row inside the 256-row tile
+            // this slice's partial block of a last-wave tile: [column][row], 256 rows
+            float* tpart = tail ? p.tail_P + (static_cast<int64_t>(tile - p.tail_first) * p.tail_split + slice) *
+                                                 (2 * Cfg::BM) * BN
+                                : nullptr;
             const int buf = lu & 1;
             const bool ready = __all_sync(
                 0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * buf, (lu >> 1) & 1, p.timeout_ns, abort_flag));
@@ -368,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                 // for the previous store (the compiler cannot rule out that they
                 // alias) and the epilogue would run at DRAM latency.
                 float* dst = p.C + jb * p.ldc + i;
-                const bool read_c = row_ok && p.split == 1 && beta != 0.0f;
+                const bool read_c = row_ok && p.split == 1 && !tail && beta != 0.0f;
                 float cv[32];
                 if (read_c && full) {
 #pragma unroll
@@ -381,7 +407,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                 tmem_ld_32x32b_x32(lane_base + 32 * c, v);
                 tmem_wait_ld();
                 if (!row_ok) continue;
-                if (p.split > 1) {
+                if (tail) {
+                    float* part = tpart + (32 * c) * (2 * Cfg::BM) + i_loc;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) part[t * (2 * Cfg::BM)] = __uint_as_float(v[t]);
+                } else if (p.split > 1) {
                     float* part = p.P + slice * p.p_stride + jb * p.ldp + i;
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
@@ -409,6 +439,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(acc_empty_leader0 + 8 * buf);  // buffer free for the next unit
+            if (tail) {
+                // Publish this slice's partials; the last slice of this warp's region
+                // to arrive sums all of them in slice order and writes C.
+                __threadfence();
+                __syncwarp();
+                int arrived = 0;
+                const int region = (tile - p.tail_first) * (2 * Cfg::EPI_WARPS) + static_cast<int>(rank) * Cfg::EPI_WARPS +
+                                   (warp - 2);
+                if (lane == 0) arrived = atomicAdd(p.tail_cnt + region, 1);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == p.tail_split - 1) {
+                    __threadfence();
+                    const float* tile0 = p.tail_P + static_cast<int64_t>(tile - p.tail_first) * p.tail_split *
+                                                        (2 * Cfg::BM) * BN;
+#pragma unroll 1
+                    for (int c = half; c < BN / 32; c += kGroups) {
+                        const int64_t jb = n0 + 32 * c;
+                        if (jb >= p.n) break;
+                        if (!row_ok) continue;
+                        const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
+                        float* dst = p.C + jb * p.ldc + i;
+                        float acc[32], cv[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            acc[t] = 0.0f;
+                            cv[t] = (beta != 0.0f && t < jn) ? dst[t * p.ldc] : 0.0f;
+                        }
+                        for (int j = 0; j < p.tail_split; ++j) {
+                            const float* src = tile0 + static_cast<int64_t>(j) * (2 * Cfg::BM) * BN +
+                                               (32 * c) * (2 * Cfg::BM) + i_loc;
+                            float pv[32];
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) pv[t] = __ldcg(src + t * (2 * Cfg::BM));
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) acc[t] += pv[t];
+                        }
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            if (t < jn) {
+                                float o = alpha * acc[t];
+                                if (beta != 0.0f) o = fmaf(beta, cv[t], o);
+                                dst[t * p.ldc] = o;
+                            }
+                        }
+                    }
+                }
+            }
         }
     }
 
@@ -462,6 +539,8 @@ struct Launcher {
 int tc2_bk(bool split3) { return split3 ? Tc2Cfg<256, true>::BK : Tc2Cfg<256, false>::BK; }
 
 int tc2_threads() { return Tc2Cfg<256, false>::THREADS; }
+
+int tc2_epilogue_warps() { return Tc2Cfg<256, false>::EPI_WARPS; }
 
 int tc2_stages(int bn, bool split3) {
     if (split3) return bn == 128 ? Tc2Cfg<128, true>::STAGES : Tc2Cfg<256, true>::STAGES;

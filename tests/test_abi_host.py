@@ -130,13 +130,30 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
     # 3xTF32 on SM pairs: a split pre-pass per operand, then the GEMM
     x = plan(8192, 8192, 8192, "3xtf32")
     assert x["prep_a_name"] == "split" and x["prep_b_name"] == "split" and x["launches"] == 3
-    assert x["workspace_bytes"] == 4 * 8192 * 8192 * 4
+    assert x["workspace_bytes"] >= 4 * 8192 * 8192 * 4  # split parts (+ last-wave partials)
     # narrow shapes (single-SM kernel): the kernel splits the operands itself in shared
     # memory with four extra warps; no pre-pass, no operand workspace
     t = plan(8192, 64, 8192, "3xtf32")
     assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
     assert t["threads"] == plan(8192, 64, 8192, "tf32")["threads"] + 128
     assert t["launches"] == 1 + (t["split_k"] > 1)
+
+
+def test_plan_last_wave_split(lib):
+    # SM pairs: 256 tiles of 256x256 over 76 pairs = 3 full waves + 28 tiles; the last
+    # wave's 28 tiles run as 2 K slices each (56 units keep the pairs busy)
+    p = plan(4096, 4096, 4096, "tf32")
+    assert p["tail_tiles"] == 28 and p["tail_split"] == 2 and p["split_k"] == 1
+    assert p["workspace_bytes"] >= 28 * 2 * 256 * 256 * 4
+    q = plan(8192, 8192, 8192, "3xtf32")
+    assert q["tail_tiles"] == 1024 - 13 * 76 and q["tail_split"] == 2
+    # no split when the tiles fill whole waves, the last wave is over half full,
+    # K is short, or the problem already uses split-K; FFMA tiles are not split
+    assert plan(256 * 19, 256 * 8, 4096, "tf32")["tail_split"] == 1          # 152 tiles = 2 waves
+    assert plan(256 * 10, 256 * 12, 4096, "tf32")["tail_split"] == 1         # 120 tiles: 44 > 76/2
+    assert plan(4096, 4096, 96, "tf32")["tail_split"] == 1                  # 3 K blocks
+    assert plan(512, 512, 8192, "tf32")["tail_split"] == 1                  # split-K instead
+    assert plan(8192, 8192, 8192, "ffma")["tail_split"] == 1
 
 
 def test_plan_skinny_k_uses_deterministic_split(lib):

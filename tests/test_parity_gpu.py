@@ -179,6 +179,26 @@ def test_pair_kernel_shapes(mode, trans, case):
         pg.force_plan(0, 0)
 
 
+@pytest.mark.parametrize("mode", ("tf32", "3xtf32"))
+@pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4000, 1100, 2048)])
+def test_last_wave_split(mode, mnk):
+    """SM pairs: tiles past the last whole wave run as K slices whose partials the
+    last slice to finish sums in slice order -- ragged edges included, beta != 0,
+    bitwise repeatable."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, ldc=m + 3, alpha=-1.25, beta=0.5, dist="normal", seed=43)
+    plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode)
+    assert plan["kernel_name"] == "tc2" and plan["tail_split"] > 1, plan
+    A, B, C = synth.make(p)
+    out1, ok1 = H.run_gpu(p, mode, A, B, C)
+    out2, ok2 = H.run_gpu(p, mode, A, B, C)
+    assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, out1), cref, den, oracle.TOL[mode])
+    assert res["ok"], res
+    assert H.padding_intact(p, out1, C)
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
                                  (128, 256, 32), (257, 513, 1031), (64, 64, 200000), (160, 200, 300), (288, 130, 77),
