@@ -382,12 +382,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
             tc_fence_after_sync();
             const int64_t i = m0 + Cfg::BM * rank + 32 * q + lane;
             const bool row_ok = i < p.m;
+            // all 32 rows of this warp inside C: chunks that are also whole in n take
+            // the short path below (no predicates, pointer stepping)
+            const bool rows_whole = m0 + Cfg::BM * rank + 32 * q + 32 <= p.m;
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
 #pragma unroll 1
             for (int c = half; c < BN / 32; c += kGroups) {
                 const int64_t jb = n0 + 32 * c;
                 if (jb >= p.n) break;  // uniform across the warp
                 const bool full = p.n - jb >= 32;
+                if (full && rows_whole && !tail && p.split == 1) {
+                    // C(i, jb + t) for t < 32, all inside C; reads of C first (when beta != 0)
+                    float* d = p.C + jb * p.ldc + i;
+                    const int64_t ldc = p.ldc;
+                    uint32_t v[32];
+                    if (beta == 0.0f) {
+                        tmem_ld_32x32b_x32(lane_base + 32 * c, v);
+                        tmem_wait_ld();
+                        if (alpha == 1.0f) {
+#pragma unroll
+                            for (int t = 0; t < 32; ++t, d += ldc) *d = __uint_as_float(v[t]);
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 32; ++t, d += ldc) *d = alpha * __uint_as_float(v[t]);
+                        }
+                    } else {
+                        float cv[32];
+                        const float* s = d;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t, s += ldc) cv[t] = *s;
+                        tmem_ld_32x32b_x32(lane_base + 32 * c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t, d += ldc) *d = fmaf(beta, cv[t], alpha * __uint_as_float(v[t]));
+                    }
+                    continue;
+                }
                 const int jn = full ? 32 : static_cast<int>(p.n - jb);
                 // All 32 loads of C are issued before the tensor-memory read and
                 // before any store: interleaved with the stores, each load would wait
@@ -396,13 +426,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                 float* dst = p.C + jb * p.ldc + i;
                 const bool read_c = row_ok && p.split == 1 && !tail && beta != 0.0f;
                 float cv[32];
-                if (read_c && full) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) cv[t] = dst[t * p.ldc];
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
-                }
+                for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_base + 32 * c, v);
                 tmem_wait_ld();
@@ -416,15 +441,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
                         if (t < jn) part[t * p.ldp] = __uint_as_float(v[t]);
-                } else if (full) {
-                    // whole chunk: no per-column predicate; beta == 0 reads nothing
-                    if (beta == 0.0f) {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) dst[t * p.ldc] = alpha * __uint_as_float(v[t]);
-                    } else {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) dst[t * p.ldc] = fmaf(beta, cv[t], alpha * __uint_as_float(v[t]));
-                    }
                 } else {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
