@@ -121,14 +121,14 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
 
 // Split the BYTES of FP32 values at `tile` (shared memory, TMA-written) in
 // place: each value becomes its TF32 big part and its remainder goes to the same
-// offset at tile + small_offset.  A swizzled layout is a function of the byte
-// address inside 1 KiB-aligned atoms, so with both regions 1 KiB aligned the
-// remainder tile has the layout of the big one.  Thread t of NTHREADS takes the
-// 16-byte chunks t, t + NTHREADS, ... (a warp covers 512 contiguous bytes) and
-// loads all of its chunks before it stores any: a load that might alias an
-// earlier store of the same thread would otherwise wait for it.
+// offset in `small`.  A swizzled layout is a function of the byte address inside
+// 1 KiB-aligned atoms, so with both regions 1 KiB aligned the remainder tile has
+// the layout of the big one.  Thread t of NTHREADS takes the 16-byte chunks t,
+// t + NTHREADS, ... (a warp covers 512 contiguous bytes) and loads all of its
+// chunks before it stores any: a load that might alias an earlier store of the
+// same thread would otherwise wait for it.
 template <int BYTES, int NTHREADS>
-__device__ __forceinline__ void split_tile_in_place(uint8_t* tile, int small_offset, int t) {
+__device__ __forceinline__ void split_tile_in_place(uint8_t* tile, uint8_t* small, int t) {
     static_assert(BYTES % (16 * NTHREADS) == 0, "whole chunks per thread");
     constexpr int CH = BYTES / (16 * NTHREADS);
     float4 v[CH];
@@ -142,7 +142,7 @@ __device__ __forceinline__ void split_tile_in_place(uint8_t* tile, int small_off
         split_tf32(v[c].z, v[c].z, sm.z);
         split_tf32(v[c].w, v[c].w, sm.w);
         *reinterpret_cast<float4*>(tile + 16 * (t + c * NTHREADS)) = v[c];
-        *reinterpret_cast<float4*>(tile + small_offset + 16 * (t + c * NTHREADS)) = sm;
+        *reinterpret_cast<float4*>(small + 16 * (t + c * NTHREADS)) = sm;
     }
 }
 

@@ -29,15 +29,16 @@
 //     rows with the 64-byte swizzle (groups of 512 B).  The k-step kk starts at
 //     +32*kk bytes inside the swizzle atom.
 //
-// 3xTF32 (SPLIT3): TMA brings the FP32 tiles of A and B into the "big" halves
-// of the slot; four transform warps then split every value in place into its
-// TF32 "big" part and write the exact remainder ("small") at the same offset of
-// the slot's other half, fence the generic-proxy writes for the tensor core and
-// arrive on the slot's "ready" barrier, which the MMA thread waits for.  Per
-// k-step it issues small*big, big*small, big*big into the same accumulator (the
-// small*small term is below FP32 resolution and dropped).  Four operand tiles
-// per slot halve BK to 16 so four slots still fit; only half of each slot comes
-// from memory, so 3xTF32 reads each operand byte from DRAM once, like TF32.
+// 3xTF32 (SPLIT3): TMA brings the FP32 tiles of A and B into the ring's slots
+// exactly as for TF32; four transform warps then split every value in place into
+// its TF32 "big" part and write the exact remainder ("small") at the same offset
+// of a slot of a second, short ring (1-2 slots), fence the generic-proxy writes
+// for the tensor core and arrive on the slot's "ready" barrier, which the MMA
+// thread waits for.  Per k-step it issues small*big, big*small, big*big into the
+// same accumulator (the small*small term is below FP32 resolution and dropped),
+// then releases both slots.  3xTF32 thus reads each operand byte from DRAM once,
+// like TF32, and the remainders occupy only the short ring, so most of shared
+// memory still holds operand bytes in flight (these shapes are HBM-bound).
 //
 // Every wait is bounded; on expiry the CTA records the status, lets its
 // in-flight TMA copies and MMAs finish (bounded), frees TMEM and exits.
@@ -53,21 +54,23 @@ namespace {
 template <int BN, bool SPLIT3>
 struct TcCfg {
     static constexpr int BM = kBM;
-    static constexpr int BK = SPLIT3 ? 16 : 32;
-    static constexpr int OPS = SPLIT3 ? 2 : 1;   // parts per operand
-    static constexpr int A_BYTES = BM * BK * 4;  // one part of A
-    static constexpr int B_BYTES = BN * BK * 4;  // one part of B
+    static constexpr int BK = 32;
+    static constexpr int A_BYTES = BM * BK * 4;  // A tile of a slot
+    static constexpr int B_BYTES = BN * BK * 4;  // B tile of a slot
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
-    static constexpr int STAGE_BYTES = OPS * (A_BYTES + B_BYTES);
-    static constexpr int TMA_BYTES = A_BYTES + B_BYTES;  // FP32 tiles loaded per slot
-    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // FP32 tiles loaded per slot
+    // 3xTF32 remainder ring: 2 slots (1 for the 256-wide tile, whose slots are largest)
+    static constexpr int SMALL_STAGES = !SPLIT3 ? 0 : (BN == 256 ? 1 : 2);
+    static constexpr int STAGES_RAW = (200 * 1024 - SMALL_STAGES * STAGE_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr int XF_WARPS = SPLIT3 ? 4 : 0;      // transform warps
     static constexpr int THREADS = 192 + 32 * XF_WARPS;
-    static constexpr int BAR_BYTES = (3 * STAGES + 1) * 8 + 16;
-    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static constexpr int BAR_BYTES = (3 * STAGES + SMALL_STAGES + 1) * 8 + 16;
+    static constexpr size_t SMEM =
+        1024 + static_cast<size_t>(STAGES + SMALL_STAGES) * STAGE_BYTES + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = BN;  // power of two >= 32
-    static_assert(STAGES >= 2, "ring too shallow");
+    static_assert(STAGES >= 2 && (STAGES >= 3 || !SPLIT3), "ring too shallow");
+    static_assert(SMEM <= 232448, "over the 227 KiB of dynamic shared memory per CTA");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
 };
@@ -80,14 +83,17 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
-    // [0,S) full, [S,2S) empty, 2S accum, [2S+1, 3S+1) ready (3xTF32)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 1);
+    constexpr int SS = Cfg::SMALL_STAGES;
+    uint8_t* small_ring = smem + S * Cfg::STAGE_BYTES;  // 3xTF32 remainders, SS slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (S + SS) * Cfg::STAGE_BYTES);
+    // [0,S) full, [S,2S) empty, 2S accum, [2S+1, 3S+1) ready, [3S+1, 3S+1+SS) small_empty
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 1 + SS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + S);
     const uint32_t accum_bar = smem_u32(bars + 2 * S);
     const uint32_t ready0 = smem_u32(bars + 2 * S + 1);
+    const uint32_t small_empty0 = smem_u32(bars + 3 * S + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -106,6 +112,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             mbar_init(empty0 + 8 * s, 1);
             if (SPLIT3) mbar_init(ready0 + 8 * s, Cfg::XF_WARPS);
         }
+        for (int j = 0; j < SS; ++j) mbar_init(small_empty0 + 8 * j, 1);
         mbar_init(accum_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                         break;
                     }
                     const uint32_t full = full0 + 8 * s;
-                    mbar_arrive_expect_tx(full, Cfg::TMA_BYTES);
+                    mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
                     const int32_t kc = (kb0 + it) * Cfg::BK;
                     const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
                     // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
@@ -165,9 +172,8 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                                             full);
                         }
                     };
-                    // FP32 tiles into the big halves: [A big][A small][B big][B small]
                     load_a(slot, &tmA);
-                    load_b(slot + Cfg::OPS * Cfg::A_BYTES, &tmB);
+                    load_b(slot + Cfg::A_BYTES, &tmB);
                     issued = it + 1;
                 }
             }
@@ -189,10 +195,12 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+                const int j = SS > 0 ? it % SS : 0;  // remainder slot (3xTF32)
+                const uint32_t small = smem_u32(small_ring + j * Cfg::STAGE_BYTES);
                 const uint32_t a_big = slot;
-                const uint32_t a_small = slot + Cfg::A_BYTES;
-                const uint32_t b_big = slot + Cfg::OPS * Cfg::A_BYTES;
-                const uint32_t b_small = b_big + Cfg::B_BYTES;
+                const uint32_t a_small = small;
+                const uint32_t b_big = slot + Cfg::A_BYTES;
+                const uint32_t b_small = small + Cfg::A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
                     const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
@@ -210,6 +218,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     }
                 }
                 mma_commit(empty0 + 8 * s);  // slot reusable once these MMAs have read it
+                if (SPLIT3) mma_commit(small_empty0 + 8 * j);  // and so is the remainder slot
             }
             mma_commit(accum_bar);  // accumulator complete (also after an abort)
         }
@@ -220,15 +229,21 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             const int t = threadIdx.x - 192;
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
+                const int j = it % SS;
+                // the slot has landed, and the MMAs of k-block it - SS have released
+                // remainder slot j
                 const bool landed = __all_sync(
-                    0xffffffffu, mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag));
+                    0xffffffffu,
+                    mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag) &&
+                        mbar_wait_bounded(small_empty0 + 8 * j, ((it / SS) & 1) ^ 1, p.timeout_ns, abort_flag));
                 if (!landed) {
                     if (lane == 0) raise_abort(abort_flag, p.status);
                     break;
                 }
                 uint8_t* slot = smem + s * Cfg::STAGE_BYTES;
-                split_tile_in_place<Cfg::A_BYTES, 32 * Cfg::XF_WARPS>(slot, Cfg::A_BYTES, t);
-                split_tile_in_place<Cfg::B_BYTES, 32 * Cfg::XF_WARPS>(slot + 2 * Cfg::A_BYTES, Cfg::B_BYTES, t);
+                uint8_t* small = small_ring + j * Cfg::STAGE_BYTES;
+                split_tile_in_place<Cfg::A_BYTES, 32 * Cfg::XF_WARPS>(slot, small, t);
+                split_tile_in_place<Cfg::B_BYTES, 32 * Cfg::XF_WARPS>(slot + Cfg::A_BYTES, small + Cfg::A_BYTES, t);
                 fence_proxy_async_smem();  // the tensor core reads these writes
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ready0 + 8 * s);
