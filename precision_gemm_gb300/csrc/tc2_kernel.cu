@@ -68,6 +68,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive without release semantics: for signals that publish no memory writes.
+// The epilogue frees a TMEM accumulator buffer with it once tcgen05.wait::ld has
+// returned (the buffer is no longer read); a release arrive would first wait
+// for all of the warp's outstanding stores of C to be performed.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // TMA tile load into this CTA's shared memory that completes on the mbarrier at
 // `bar_cluster` (CTA 0 of the pair).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
@@ -454,7 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(acc_empty_leader0 + 8 * buf);  // buffer free for the next unit
+            if (lane == 0) mbar_arrive_remote_relaxed(acc_empty_leader0 + 8 * buf);  // buffer free for the next unit
             if (tail) {
                 // Publish this slice's partials; the last slice of this warp's region
                 // to arrive sums all of them in slice order and writes C.
