@@ -29,6 +29,12 @@
 // the MMA completion is multicast), acc_full[b] (both CTAs; multicast),
 // acc_empty[b] (CTA 0; arrived by the 16 epilogue warps of the pair).
 //
+// 3xTF32: A and B arrive split by a pre-pass into TF32 "big" parts and exact
+// remainders (four tensor maps); each ring slot holds all four tiles at BK 16 and
+// the MMA thread issues small*big, big*small, big*big per k-step.  (Splitting in
+// shared memory instead, as the single-SM kernel does for its narrow shapes,
+// measured 2.3x slower here: the transform's latency joins every slot's round trip.)
+//
 // Shared-memory layouts are those of the single-SM kernel (tc_kernel.cu): A
 // M-major in the 128-byte swizzle with 32-byte atoms, B K-major in the 128-byte
 // (BK 32) or 64-byte (BK 16) swizzle.  In the pair the descriptors name

@@ -11,7 +11,8 @@
 // barriers have nothing left to order.
 //
 // Warp roles (192 threads; 320 in 3xTF32):
-//   warp 0      TMA loader (one thread): A as four 32-row boxes, B as one box
+//   warp 0      TMA loader (one thread): A as one box (K-major, or M-major as one
+//               3-D box of four 32-row groups) or four 32-row boxes; B likewise
 //   warp 1      allocates TMEM; one thread issues the MMAs; frees TMEM at exit
 //   warps 2-5   epilogue; warp w may access TMEM lanes 32*(w%4) .. +31
 //   warps 6-9   3xTF32 only: split each landed slot into TF32 parts
