@@ -4,7 +4,8 @@
 //     A M-major and B K-major), transposing it when trans = 'T', and for 3xTF32
 //     splitting every value into a TF32 "big" part and its exact remainder;
 //   * the split-K reduction C = alpha * sum_s P[s] + beta * C, slices summed in
-//     increasing s (deterministic);
+//     a fixed order (increasing s; with many slices, four contiguous groups in
+//     increasing s, then the groups in order) -- deterministic;
 //   * C = beta * C for calls with k == 0 or alpha == 0.
 // All are bound by HBM bandwidth: grids are sized as a multiple of the SM count
 // and every warp touches 128 contiguous bytes per access where the layout allows.
@@ -170,6 +171,53 @@ __global__ void __launch_bounds__(256, 4) splitk_reduce_kernel(const GemmParams 
     }
 }
 
+// The same reduction when there are many slices and few outputs (a 128 x 128
+// result split 152 ways): a thread summing all S slices of one output would be
+// bound by DRAM latency, so kG threads share each output.  Thread g sums the
+// contiguous slices [g*S/kG, (g+1)*S/kG) in increasing order (kS loads in
+// flight) and the kG partial sums are then added in increasing g -- a fixed
+// association, so the result does not depend on scheduling.  A CTA covers 64
+// consecutive rows of one column.
+constexpr int kG = 4;
+
+__global__ void __launch_bounds__(256) splitk_reduce_grouped_kernel(const GemmParams p) {
+    __shared__ float part[kG][64];
+    const int rl = threadIdx.x & 63;
+    const int g = threadIdx.x >> 6;
+    const int s0 = (g * p.split) / kG, s1 = ((g + 1) * p.split) / kG;
+    const float* __restrict__ P = p.P;
+    float* __restrict__ C = p.C;
+    for (int64_t c = blockIdx.y; c < p.n; c += gridDim.y) {
+        for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64; r0 < p.m; r0 += static_cast<int64_t>(gridDim.x) * 64) {
+            const int64_t r = r0 + rl;
+            float acc = 0.0f;
+            if (r < p.m) {
+                const float* ps = P + c * p.ldp + r;
+                int s = s0;
+                for (; s + kS <= s1; s += kS) {
+                    float v[kS];
+#pragma unroll
+                    for (int q = 0; q < kS; ++q) v[q] = ps[(s + q) * p.p_stride];
+#pragma unroll
+                    for (int q = 0; q < kS; ++q) acc += v[q];
+                }
+                for (; s < s1; ++s) acc += ps[s * p.p_stride];
+            }
+            part[g][rl] = acc;
+            __syncthreads();
+            if (g == 0 && r < p.m) {
+                float sum = part[0][rl];
+#pragma unroll
+                for (int q = 1; q < kG; ++q) sum += part[q][rl];
+                float o = p.alpha * sum;
+                if (p.beta != 0.0f) o = fmaf(p.beta, C[c * p.ldc + r], o);
+                C[c * p.ldc + r] = o;
+            }
+            __syncthreads();
+        }
+    }
+}
+
 // C = beta * C (beta = 0 writes zeros without reading C).
 __global__ void __launch_bounds__(256, 4) scale_kernel(float* __restrict__ C, int64_t ldc, int64_t m, int64_t n,
                                                        float beta, int tx_shift, int by_rows) {
@@ -234,6 +282,17 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
 }
 
 cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t stream) {
+    if (p.split >= 8 * kG) {  // every thread group still sums at least kS slices
+        const int64_t row_blocks = (p.m + 63) / 64;
+        const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+        int64_t by = p.n < 65535 ? p.n : 65535;
+        int64_t bx = (target + by - 1) / by;
+        if (bx > row_blocks) bx = row_blocks;
+        if (bx < 1) bx = 1;
+        splitk_reduce_grouped_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by)), 256, 0, stream>>>(
+            p);
+        return cudaGetLastError();
+    }
     int sh = 8, by_rows = 0;
     const dim3 grid = sweep_grid(p.m, p.n, num_sms, &sh, &by_rows);
     splitk_reduce_kernel<<<grid, 256, 0, stream>>>(p, sh);
