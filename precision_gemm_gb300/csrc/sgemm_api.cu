@@ -184,8 +184,12 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->k_blocks = static_cast<int>(cdiv(k, pl->bk));
 
     // Split-K when the output tiles cannot fill one wave of the machine: give
-    // each tile floor(capacity / tiles) K slices of at least 4 K blocks each
-    // (capacity counts SM pairs for the pair kernel).
+    // each tile up to floor(capacity / tiles) K slices (capacity counts SM pairs
+    // for the pair kernel).  A slice must carry enough work to repay the partial
+    // sums' round trip and the reduction launch, which the tensor cores reach
+    // only with longer K: FFMA splits into slices of at least 128 of K; TF32 only
+    // when K >= 2048, into slices of at least 512; 3xTF32 only when K >= 512,
+    // into slices of at least 128 (measured on 256^3 .. 2048^3, K up to 262144).
     const int64_t tiles = static_cast<int64_t>(pl->tiles_m) * pl->tiles_n;
     const int64_t capacity =
         pair ? std::max(num_sms / 2, 1) : static_cast<int64_t>(std::max(num_sms, 1)) * pl->ctas_per_sm;
@@ -193,8 +197,11 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     const int fs = g_force_split.load();
     if (fs > 0) {
         split = fs;
-    } else if (tiles < capacity) {
-        split = std::min<int64_t>(capacity / tiles, pl->k_blocks / 4);
+    } else {
+        const int64_t min_k_slice = (tc && !split3) ? 512 : 128;
+        const int64_t min_k_total = !tc ? 0 : (split3 ? 512 : 2048);
+        if (tiles < capacity && k >= min_k_total)
+            split = std::min<int64_t>(capacity / tiles, pl->k_blocks / cdiv(min_k_slice, pl->bk));
     }
     split = std::max<int64_t>(1, std::min<int64_t>({split, static_cast<int64_t>(pl->k_blocks), 65535}));
     const int64_t per = cdiv(pl->k_blocks, split);
