@@ -135,8 +135,12 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     const bool split3 = mode == SGEMM_3XTF32;
 
     // Tile width: 64 for n <= 64; otherwise 128 for the FFMA kernel (two CTAs per
-    // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05.
+    // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05 --
+    // except that a tensor-core product whose 128 x 64 tiles fit in one wave of
+    // SMs runs on those (single-SM kernel): lowest latency up to ~1024^3, and
+    // 3xTF32 there splits in shared memory instead of running two pre-passes.
     int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
+    if (tc && cdiv(m, kBM) * cdiv(n, 64) <= std::max(num_sms, 1)) bn = 64;
     const int fbn = g_force_bn.load();
     if (fbn) bn = fbn;
     pl->bn = bn;

@@ -167,12 +167,18 @@ def test_plan_skinny_k_uses_deterministic_split(lib):
 
 
 def test_plan_pair_kernel_only_above_128_rows(lib):
-    assert plan(128, 4096, 4096, "tf32")["kernel_name"] == "tc"       # one SM tile covers m
-    assert plan(129, 4096, 4096, "tf32")["kernel_name"] == "tc2"
+    assert plan(128, 8192, 4096, "tf32")["kernel_name"] == "tc"       # one SM tile covers m
+    assert plan(129, 8192, 4096, "tf32")["kernel_name"] == "tc2"
     assert plan(4096, 64, 4096, "3xtf32")["kernel_name"] == "tc"      # 64-wide tile: single SM
-    small = plan(512, 512, 65536, "tf32")                              # 2 x 2 pair tiles -> split K over 76 pairs
-    assert small["kernel_name"] == "tc2" and small["tiles_m"] * small["tiles_n"] == 4
-    assert small["split_k"] == 76 // 4
+    # products whose 128 x 64 tiles fit one wave of SMs run on those (lowest latency)
+    small = plan(512, 512, 65536, "tf32")                              # 4 x 8 tiles -> split K over 152 SMs
+    assert small["kernel_name"] == "tc" and small["bn"] == 64 and small["tiles_m"] * small["tiles_n"] == 32
+    assert small["split_k"] == 152 // 32
+    assert plan(1024, 1024, 1024, "3xtf32")["kernel_name"] == "tc"     # 128 tiles: one wave
+    assert plan(1536, 1536, 1536, "3xtf32")["kernel_name"] == "tc2"    # 288 tiles: SM pairs
+    pair = plan(1280, 1280, 65536, "tf32")                             # 5 x 5 pair tiles -> split K over 76 pairs
+    assert pair["kernel_name"] == "tc2" and pair["tiles_m"] * pair["tiles_n"] == 25
+    assert pair["split_k"] == 76 // 25
 
 
 def test_plan_misaligned_ld_copies_operand(lib):
@@ -193,8 +199,8 @@ def test_plan_transposed_operands(lib):
     assert t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
     assert t["ld_a"] == 104 and t["ld_b"] == 204 and t["launches"] == 1
     # 3xTF32 on SM pairs splits them without transposing: ld is the stored row count rounded to 4
-    x = plan(300, 200, 101, "3xtf32", transa="T", transb="T")
-    assert x["prep_a_name"] == "split" and x["ld_a"] == 104 and x["ld_b"] == 200
+    x = plan(3000, 2000, 101, "3xtf32", transa="T", transb="T")
+    assert x["kernel_name"] == "tc2" and x["prep_a_name"] == "split" and x["ld_a"] == 104 and x["ld_b"] == 2000
     # the single-SM kernel reads them in place and splits in shared memory; a stored
     # row count that is not a multiple of 4 still needs a plain copy, ld rounded up
     y = plan(100, 64, 101, "3xtf32", transa="T", transb="T")

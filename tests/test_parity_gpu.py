@@ -157,12 +157,13 @@ def test_transposed_operands_read_in_place(mode, trans, mnk):
 @pytest.mark.parametrize("mode", ("tf32", "3xtf32"))
 @pytest.mark.parametrize("trans", ["NN", "NT", "TN", "TT"])
 @pytest.mark.parametrize("case", [
-    # (m, n, k, forced bn): SM-pair tiles with ragged rows/columns and split-K
-    (1024, 1024, 512, 0),
+    # (m, n, k, forced bn): SM-pair tiles with ragged rows/columns and split-K (the
+    # smaller shapes would run on single-SM 128 x 64 tiles unless bn is forced)
+    (1024, 1024, 512, 256),
     (700, 2148, 300, 0),
-    (640, 640, 1000, 0),
+    (640, 640, 1000, 256),
     (1000, 512, 777, 128),   # 128-wide pair tiles, 2-D A boxes when M-major
-    (512, 512, 8192, 0),     # split-K on the pair kernel
+    (512, 512, 8192, 256),   # split-K on the pair kernel
 ])
 def test_pair_kernel_shapes(mode, trans, case):
     """The SM-pair kernel (256-row tiles) with every operand orientation,
