@@ -139,8 +139,14 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // except that a tensor-core product whose 128 x 64 tiles fit in one wave of
     // SMs runs on those (single-SM kernel): lowest latency up to ~1024^3, and
     // 3xTF32 there splits in shared memory instead of running two pre-passes.
+    // Tiny FFMA products (under 2 GFLOP, their 128 x 64 tiles filling at most half
+    // the SMs) take the 64-wide tile too, with thinner K slices below: more CTAs
+    // share the few k-blocks.
     int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
-    if (tc && cdiv(m, kBM) * cdiv(n, 64) <= std::max(num_sms, 1)) bn = 64;
+    const int64_t tiles64 = cdiv(m, kBM) * cdiv(n, 64);
+    if (tc && tiles64 <= std::max(num_sms, 1)) bn = 64;
+    const bool tiny_ffma = !tc && 2 * tiles64 <= std::max(num_sms, 1) && 2.0 * m * n * k <= 2e9;
+    if (tiny_ffma) bn = 64;
     const int fbn = g_force_bn.load();
     if (fbn) bn = fbn;
     pl->bn = bn;
@@ -193,7 +199,8 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // sums' round trip and the reduction launch, which the tensor cores reach
     // only with longer K: FFMA splits into slices of at least 128 of K; TF32 only
     // when K >= 2048, into slices of at least 512; 3xTF32 only when K >= 512,
-    // into slices of at least 128 (measured on 256^3 .. 2048^3, K up to 262144).
+    // into slices of at least 128; tiny FFMA products into slices of 64
+    // (measured on 256^3 .. 2048^3, K up to 262144).
     const int64_t tiles = static_cast<int64_t>(pl->tiles_m) * pl->tiles_n;
     const int64_t capacity =
         pair ? std::max(num_sms / 2, 1) : static_cast<int64_t>(std::max(num_sms, 1)) * pl->ctas_per_sm;
@@ -202,7 +209,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     if (fs > 0) {
         split = fs;
     } else {
-        const int64_t min_k_slice = (tc && !split3) ? 512 : 128;
+        const int64_t min_k_slice = (tc && !split3) ? 512 : (tiny_ffma ? 64 : 128);
         const int64_t min_k_total = !tc ? 0 : (split3 ? 512 : 2048);
         if (tiles < capacity && k >= min_k_total)
             split = std::min<int64_t>(capacity / tiles, pl->k_blocks / cdiv(min_k_slice, pl->bk));
