@@ -118,3 +118,32 @@ def test_host_async_calls_overlap_and_match_sync(same_stream):
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), (p, mode)
         _check(p, mode, A, B, C, out)
     assert pg.device_status() == 0
+
+
+@pytest.mark.parametrize("mode", ("tf32", "3xtf32"))
+def test_captured_last_wave_split_replays(mode):
+    """A product that splits its last wave along K (arrival counters zeroed by a
+    memset before the kernel) captured into a graph: every replay starts from
+    zeroed counters and gives the same bits."""
+    p = synth.Problem(2500, 2000, 1000, alpha=1.0, beta=0.5, dist="normal", seed=71)
+    plan = pg.sgemm_plan("N", "N", p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode)
+    assert plan["tail_split"] > 1, plan
+    A, B, C = synth.make(p)
+    s = torch.cuda.Stream()
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    with torch.cuda.stream(s):
+        pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    s.synchronize()
+    first = dC.cpu()
+    _check(p, mode, A, B, C, first)
+    g = torch.cuda.CUDAGraph()
+    dC.copy_(C)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    for _ in range(3):
+        dC.copy_(C)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(dC.cpu().view(torch.int32), first.view(torch.int32))
+    assert pg.device_status() == 0
