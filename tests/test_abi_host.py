@@ -170,10 +170,15 @@ def test_plan_pair_kernel_only_above_128_rows(lib):
     assert plan(128, 8192, 4096, "tf32")["kernel_name"] == "tc"       # one SM tile covers m
     assert plan(129, 8192, 4096, "tf32")["kernel_name"] == "tc2"
     assert plan(4096, 64, 4096, "3xtf32")["kernel_name"] == "tc"      # 64-wide tile: single SM
-    # products whose 128 x 64 tiles fit one wave of SMs run on those (lowest latency)
-    small = plan(512, 512, 65536, "tf32")                              # 4 x 8 tiles -> split K over 152 SMs
+    # small products whose 128 x 64 tiles fit one wave of SMs run on those (lowest latency)
+    small = plan(512, 512, 4096, "tf32")                               # 4 x 8 tiles -> split K over 152 SMs
     assert small["kernel_name"] == "tc" and small["bn"] == 64 and small["tiles_m"] * small["tiles_n"] == 32
     assert small["split_k"] == 152 // 32
+    long_k = plan(512, 512, 65536, "tf32")                             # long K: SM pairs, 2 x 2 tiles, split K
+    assert long_k["kernel_name"] == "tc2" and long_k["split_k"] == 76 // 4
+    # 3xTF32 keeps the single-SM kernel at any K (its split in shared memory avoids two pre-passes)
+    assert plan(8192, 128, 8192, "3xtf32")["kernel_name"] == "tc"
+    assert plan(8192, 128, 8192, "tf32")["kernel_name"] == "tc2"
     assert plan(1024, 1024, 1024, "3xtf32")["kernel_name"] == "tc"     # 128 tiles: one wave
     assert plan(1536, 1536, 1536, "3xtf32")["kernel_name"] == "tc2"    # 288 tiles: SM pairs
     pair = plan(1280, 1280, 65536, "tf32")                             # 5 x 5 pair tiles -> split K over 76 pairs
