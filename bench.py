@@ -411,11 +411,13 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--fma-ceiling", action="store_true",
                     help="run only the register-only FP32 FMA throughput probe and print its JSON line")
+    ap.add_argument("--tf32-ceiling", action="store_true",
+                    help="run only the shared-memory-resident tcgen05 TF32 throughput probe and print its JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
-    if args.fma_ceiling:
+    if args.fma_ceiling or args.tf32_ceiling:
         from precision_gemm_gb300 import build as pgbuild
-        subprocess.run([pgbuild.build_probe()], check=True)
+        subprocess.run([pgbuild.build_probe("fma_ceiling" if args.fma_ceiling else "tf32_ceiling")], check=True)
         return
     if args.impl == "reference":
         line = run_reference(args, args.workload)

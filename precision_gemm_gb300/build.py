@@ -71,16 +71,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
-PROBE_SRC = os.path.join(HERE, "probes", "fma_ceiling.cu")
-PROBE_BIN = os.path.join(HERE, "probes", "fma_ceiling")
+PROBES = ("fma_ceiling", "tf32_ceiling")
 
 
-def build_probe(force: bool = False) -> str:
-    """Compile the register-only FMA ceiling probe (a small executable)."""
-    if not force and os.path.exists(PROBE_BIN) and os.path.getmtime(PROBE_BIN) >= os.path.getmtime(PROBE_SRC):
-        return PROBE_BIN
-    subprocess.run([_nvcc(), *ARCH, "-O3", "-o", PROBE_BIN, PROBE_SRC], check=True)
-    return PROBE_BIN
+def build_probe(name: str = "fma_ceiling", force: bool = False) -> str:
+    """Compile a throughput probe (a small executable): the register-only FMA
+    ceiling or the shared-memory-resident tcgen05 TF32 ceiling."""
+    src = os.path.join(HERE, "probes", name + ".cu")
+    binary = os.path.join(HERE, "probes", name)
+    deps = [src] + ([os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h")] if name == "tf32_ceiling" else [])
+    if not force and os.path.exists(binary) and all(os.path.getmtime(binary) >= os.path.getmtime(d) for d in deps):
+        return binary
+    subprocess.run([_nvcc(), *ARCH, "-O3", "-std=c++17", "-o", binary, src], check=True)
+    return binary
 
 
 if __name__ == "__main__":
