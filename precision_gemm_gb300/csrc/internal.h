@@ -65,7 +65,7 @@ cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
 // HBM traffic than the product).
 int tc_bk(bool split3);
 int tc_stages(int bn, bool split3);
-int tc_threads(bool split3);
+int tc_threads(int bn, bool split3);
 size_t tc_smem_bytes(int bn, bool split3);
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, bool split3,
                       dim3 grid, cudaStream_t stream);

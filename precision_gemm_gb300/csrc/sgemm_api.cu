@@ -188,7 +188,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->bm = pair ? 2 * kBM : kBM;
     pl->bk = !tc ? kFfmaBK : (pair ? tc2_bk(split3) : tc_bk(split3));
     pl->stages = !tc ? ffma_stages(bn) : (pair ? tc2_stages(bn, split3) : tc_stages(bn, split3));
-    pl->threads = !tc ? ffma_threads(bn) : (pair ? tc2_threads() : tc_threads(split3));
+    pl->threads = !tc ? ffma_threads(bn) : (pair ? tc2_threads() : tc_threads(bn, split3));
     pl->ctas_per_sm = tc ? 1 : ffma_ctas_per_sm(bn);
     pl->smem_bytes = !tc ? ffma_smem_bytes(bn) : (pair ? tc2_smem_bytes(bn, split3) : tc_smem_bytes(bn, split3));
     pl->tiles_m = static_cast<int>(cdiv(m, pl->bm));
@@ -420,10 +420,13 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
         gp.b_mnmajor = b_mnmajor ? 1 : 0;
         gp.a3d = (!a_kmajor && m % 32 == 0) ? 1 : 0;
         gp.b3d = (b_mnmajor && n % 32 == 0) ? 1 : 0;
+        // The single-SM 3xTF32 kernel splits A into tensor memory: its M-major A
+        // tile is read only by threads, so it lands without a swizzle.
+        const CUtensorMapSwizzle msw_a = (!pair && split3) ? CU_TENSOR_MAP_SWIZZLE_NONE : msw;
         auto encode_a = [&](CUtensorMap* map, const float* base) {
             if (a_kmajor) return encode_2d(map, base, k, m, pl.ld_a, pl.bk, kBM, ksw);
-            return gp.a3d ? encode_mn3d(map, base, m, k, pl.ld_a, pl.bk, 4, msw)
-                          : encode_2d(map, base, m, k, pl.ld_a, 32, pl.bk, msw);
+            return gp.a3d ? encode_mn3d(map, base, m, k, pl.ld_a, pl.bk, 4, msw_a)
+                          : encode_2d(map, base, m, k, pl.ld_a, 32, pl.bk, msw_a);
         };
         auto encode_b = [&](CUtensorMap* map, const float* base) {
             if (!b_mnmajor) return encode_2d(map, base, k, n, pl.ld_b, pl.bk, b_cols, ksw);

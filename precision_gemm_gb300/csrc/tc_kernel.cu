@@ -10,12 +10,14 @@
 // thread replaces per-warp MMA fragments, so the pages' per-warp "shift"
 // barriers have nothing left to order.
 //
-// Warp roles (192 threads; 320 in 3xTF32):
+// Warp roles (192 threads; 320 or 448 in 3xTF32):
 //   warp 0      TMA loader (one thread): A as one box (K-major, or M-major as one
 //               3-D box of four 32-row groups) or four 32-row boxes; B likewise
 //   warp 1      allocates TMEM; one thread issues the MMAs; frees TMEM at exit
 //   warps 2-5   epilogue; warp w may access TMEM lanes 32*(w%4) .. +31
-//   warps 6-9   3xTF32 only: split each landed slot into TF32 parts
+//   warps 6-13  3xTF32 only: split each landed slot into TF32 parts, in one or
+//               two groups of four (warp w handles the A rows of TMEM lane
+//               quarter w % 4)
 //
 // Shared-memory operand layouts (canonical tcgen05 layouts, 1 KiB aligned):
 //   A (column-major, M-major): per 32-row group of M a box of BK rows of k,
@@ -31,15 +33,24 @@
 //     +32*kk bytes inside the swizzle atom.
 //
 // 3xTF32 (SPLIT3): TMA brings the FP32 tiles of A and B into the ring's slots
-// exactly as for TF32; four transform warps then split every value in place into
-// its TF32 "big" part and write the exact remainder ("small") at the same offset
-// of a slot of a second, short ring (1-2 slots), fence the generic-proxy writes
-// for the tensor core and arrive on the slot's "ready" barrier, which the MMA
-// thread waits for.  Per k-step it issues small*big, big*small, big*big into the
-// same accumulator (the small*small term is below FP32 resolution and dropped),
-// then releases both slots.  3xTF32 thus reads each operand byte from DRAM once,
-// like TF32, and the remainders occupy only the short ring, so most of shared
-// memory still holds operand bytes in flight (these shapes are HBM-bound).
+// as for TF32 (A M-major without swizzle: the tensor core does not read it from
+// shared memory).  Groups of four transform warps then split every value into its TF32
+// "big" part and the exact remainder ("small"):
+//   A  each thread takes one row of the 128 (its warp's TMEM lane quarter),
+//      reads the row's BK values and writes big and small with tcgen05.st into a
+//      TMEM operand stage (lane = row, one value per column: big in 32 columns,
+//      small in the next 32), from which the MMAs read A;
+//   B  split in place in the slot, remainders at the same offset of a slot of a
+//      second, short ring of B remainders.
+// They then fence their writes for the tensor core and arrive on the slot's
+// "ready" barrier, which the MMA thread waits for.  Per k-step it issues
+// small*big, big*small, big*big into the same accumulator (the small*small term
+// is below FP32 resolution and dropped), then releases the slot and the
+// remainder slot with its TMEM stage.  3xTF32 thus reads each operand byte from
+// DRAM once, like TF32 (these shapes are HBM-bound), and A's parts never pass
+// through shared memory (a split in place for A as well, the earlier form of
+// this kernel, measured 3-7 % slower on the narrow shapes).  Two groups of
+// transform warps take alternate k-blocks.
 //
 // Every wait is bounded; on expiry the CTA records the status, lets its
 // in-flight TMA copies and MMAs finish (bounded), frees TMEM and exits.
@@ -52,6 +63,11 @@
 namespace pg {
 namespace {
 
+// Transform warp groups of the 3xTF32 kernel (a compile-time tunable, 1 or 2).
+#ifndef PG_TC_XF_GROUPS
+#define PG_TC_XF_GROUPS 2
+#endif
+
 template <int BN, bool SPLIT3>
 struct TcCfg {
     static constexpr int BM = kBM;
@@ -60,17 +76,32 @@ struct TcCfg {
     static constexpr int B_BYTES = BN * BK * 4;  // B tile of a slot
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // FP32 tiles loaded per slot
-    // 3xTF32 remainder ring: 2 slots (1 for the 256-wide tile, whose slots are largest)
-    static constexpr int SMALL_STAGES = !SPLIT3 ? 0 : (BN == 256 ? 1 : 2);
-    static constexpr int STAGES_RAW = (200 * 1024 - SMALL_STAGES * STAGE_BYTES) / STAGE_BYTES;
+    // 3xTF32: B remainder slots, each with a TMEM stage of A's parts (4, 2 or 1
+    // for BN = 64, 128, 256, within 200 KiB of ring)
+    static constexpr int SMALL_STAGES = !SPLIT3 ? 0 : (BN == 256 ? 1 : (BN == 128 ? 2 : 4));
+    static constexpr int STAGES_RAW = (200 * 1024 - SMALL_STAGES * B_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-    static constexpr int XF_WARPS = SPLIT3 ? 4 : 0;      // transform warps
+    // 3xTF32 transform: groups of four warps (one per TMEM lane quarter), group g
+    // taking k-blocks g, g + XF_GROUPS, ... so that one group's per-k-block
+    // latencies (barrier waits, fences) overlap another group's arithmetic.  A
+    // group waits on barrier phases out of step with the other groups, so the
+    // phase it waits for must be at most one ahead of the barrier's current
+    // phase; see the transform loop for why XF_GROUPS <= SMALL_STAGES <= STAGES
+    // guarantees it.
+    static constexpr int XF_GROUPS = !SPLIT3 ? 0 : (PG_TC_XF_GROUPS < SMALL_STAGES ? PG_TC_XF_GROUPS : SMALL_STAGES);
+    static constexpr int XF_WARPS = 4 * XF_GROUPS;      // transform warps
     static constexpr int THREADS = 192 + 32 * XF_WARPS;
     static constexpr int BAR_BYTES = (3 * STAGES + SMALL_STAGES + 1) * 8 + 16;
     static constexpr size_t SMEM =
-        1024 + static_cast<size_t>(STAGES + SMALL_STAGES) * STAGE_BYTES + BAR_BYTES;
-    static constexpr uint32_t TMEM_COLS = BN;  // power of two >= 32
+        1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + static_cast<size_t>(SMALL_STAGES) * B_BYTES + BAR_BYTES;
+    // TMEM: the accumulator in columns [0, BN); with SPLIT3 the A operand stages
+    // at columns A_TMEM_COL + 64 j (big, then small), all 512 columns allocated
+    static constexpr uint32_t A_TMEM_COL = 256;
+    static constexpr uint32_t TMEM_COLS = SPLIT3 ? 512 : BN;  // power of two >= 32
+    static_assert(!SPLIT3 || A_TMEM_COL + 64 * SMALL_STAGES <= 512, "TMEM operand stages");
     static_assert(STAGES >= 2 && (STAGES >= 3 || !SPLIT3), "ring too shallow");
+    static_assert(!SPLIT3 || (XF_GROUPS >= 1 && XF_GROUPS <= SMALL_STAGES && SMALL_STAGES <= STAGES),
+                  "transform groups may run ahead of a barrier by at most one phase");
     static_assert(SMEM <= 232448, "over the 227 KiB of dynamic shared memory per CTA");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
@@ -85,8 +116,8 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
     constexpr int SS = Cfg::SMALL_STAGES;
-    uint8_t* small_ring = smem + S * Cfg::STAGE_BYTES;  // 3xTF32 remainders, SS slots
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (S + SS) * Cfg::STAGE_BYTES);
+    uint8_t* small_ring = smem + S * Cfg::STAGE_BYTES;  // 3xTF32 B remainders, SS slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(small_ring + SS * Cfg::B_BYTES);
     // [0,S) full, [S,2S) empty, 2S accum, [2S+1, 3S+1) ready, [3S+1, 3S+1+SS) small_empty
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 1 + SS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -111,7 +142,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
-            if (SPLIT3) mbar_init(ready0 + 8 * s, Cfg::XF_WARPS);
+            if (SPLIT3) mbar_init(ready0 + 8 * s, 4);  // the four warps of one transform group
         }
         for (int j = 0; j < SS; ++j) mbar_init(small_empty0 + 8 * j, 1);
         mbar_init(accum_bar, 1);
@@ -186,7 +217,8 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             uint32_t accumulate = 0;
-            const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
+            // A from TMEM (3xTF32) is K-major by construction
+            const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !SPLIT3 && !p.a_kmajor, p.b_mnmajor != 0);
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
                 // 3xTF32: the transform warps have split the slot
@@ -196,24 +228,23 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
-                const int j = SS > 0 ? it % SS : 0;  // remainder slot (3xTF32)
-                const uint32_t small = smem_u32(small_ring + j * Cfg::STAGE_BYTES);
+                const int j = SS > 0 ? it % SS : 0;  // remainder slot and TMEM stage (3xTF32)
                 const uint32_t a_big = slot;
-                const uint32_t a_small = small;
                 const uint32_t b_big = slot + Cfg::A_BYTES;
-                const uint32_t b_small = small + Cfg::A_BYTES;
+                const uint32_t b_small = smem_u32(small_ring + j * Cfg::B_BYTES);
+                const uint32_t ta_big = tmem + Cfg::A_TMEM_COL + 64 * j;  // lane 0, A's big parts
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-                    const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
                     const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
                     if (SPLIT3) {
-                        const uint64_t asd = operand_desc<Cfg::BK>(a_small, kk, p.a_kmajor != 0);
                         const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
-                        mma_tf32(tmem, asd, bd, idesc, accumulate);
+                        const uint32_t tab = ta_big + 8 * kk;  // k-step kk: columns 8kk .. 8kk+7
+                        mma_tf32_tmem_a(tmem, tab + 32, bd, idesc, accumulate);  // small * big
                         accumulate = 1;
-                        mma_tf32(tmem, ad, bsd, idesc, 1);
-                        mma_tf32(tmem, ad, bd, idesc, 1);
+                        mma_tf32_tmem_a(tmem, tab, bsd, idesc, 1);  // big * small
+                        mma_tf32_tmem_a(tmem, tab, bd, idesc, 1);   // big * big
                     } else {
+                        const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
                         mma_tf32(tmem, ad, bd, idesc, accumulate);
                         accumulate = 1;
                     }
@@ -227,25 +258,68 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     } else if (warp >= 6) {
         // ---------------- 3xTF32 transform (warps 6..9) ----------------
         if constexpr (SPLIT3) {
-            const int t = threadIdx.x - 192;
-            for (int it = 0; it < nkb; ++it) {
+            const int grp = (warp - 6) >> 2;
+            const int t = threadIdx.x - 192 - 128 * grp;  // thread within the group
+            const int q = warp & 3;  // TMEM lane quarter: A rows 32q .. 32q + 31
+            for (int it = grp; it < nkb; it += Cfg::XF_GROUPS) {
                 const int s = it % S;
                 const int j = it % SS;
-                // the slot has landed, and the MMAs of k-block it - SS have released
-                // remainder slot j
+                // The MMAs of k-block it - SS have released remainder slot j and its
+                // TMEM stage, then k-block it has landed.  A parity wait is exact only
+                // while the awaited phase is the barrier's current or next one.  This
+                // group's previous k-block, it - XF_GROUPS >= it - SS, already saw the
+                // release of k-block it - XF_GROUPS - SS >= it - 2 SS, so small_empty[j]
+                // is at most one phase behind.  MMAs complete in order, so once the
+                // MMAs of it - SS are done those of it - S <= it - SS are too, whose
+                // slot had landed before: full[s] is then at most one phase behind.
                 const bool landed = __all_sync(
                     0xffffffffu,
-                    mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag) &&
-                        mbar_wait_bounded(small_empty0 + 8 * j, ((it / SS) & 1) ^ 1, p.timeout_ns, abort_flag));
+                    mbar_wait_bounded(small_empty0 + 8 * j, ((it / SS) & 1) ^ 1, p.timeout_ns, abort_flag) &&
+                        mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag));
                 if (!landed) {
                     if (lane == 0) raise_abort(abort_flag, p.status);
                     break;
                 }
                 uint8_t* slot = smem + s * Cfg::STAGE_BYTES;
-                uint8_t* small = small_ring + j * Cfg::STAGE_BYTES;
-                split_tile_in_place<Cfg::A_BYTES, 32 * Cfg::XF_WARPS>(slot, small, t);
-                split_tile_in_place<Cfg::B_BYTES, 32 * Cfg::XF_WARPS>(slot + Cfg::A_BYTES, small + Cfg::A_BYTES, t);
-                fence_proxy_async_smem();  // the tensor core reads these writes
+                // A row 32q + lane: its BK values.  K-major: 128-byte row in the
+                // 128-byte swizzle (16-byte chunk c at c ^ (row % 8)), read as float4s
+                // (the 8 rows of a quarter-warp hit 8 distinct chunk positions).
+                // M-major: row group q, BK lines of 32 rows, no swizzle.
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + Cfg::A_TMEM_COL + 64 * j;
+#pragma unroll
+                for (int h = 0; h < Cfg::BK / 16; ++h) {  // 16 values of the row at a time
+                    float a[16];
+                    if (p.a_kmajor) {
+                        const uint32_t row = smem_u32(slot) + (32 * q + lane) * (Cfg::BK * 4);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float4 v = lds128(row + (((4 * h + c) ^ (lane & 7)) << 4));
+                            a[4 * c] = v.x;
+                            a[4 * c + 1] = v.y;
+                            a[4 * c + 2] = v.z;
+                            a[4 * c + 3] = v.w;
+                        }
+                    } else {
+                        const float* col = reinterpret_cast<const float*>(slot + q * Cfg::A_BOX_BYTES) + lane;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) a[k] = col[32 * (16 * h + k)];
+                    }
+                    uint32_t big[16], sml[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        float b, r;
+                        split_tf32(a[k], b, r);
+                        big[k] = __float_as_uint(b);
+                        sml[k] = __float_as_uint(r);
+                    }
+                    tmem_st_32x32b_x16(ta + 16 * h, big);
+                    tmem_st_32x32b_x16(ta + 32 + 16 * h, sml);
+                }
+                split_tile_in_place<Cfg::B_BYTES, 128>(slot + Cfg::A_BYTES,
+                                                                      small_ring + j * Cfg::B_BYTES, t);
+                tmem_wait_st();
+                fence_proxy_async_smem();  // the tensor core reads the B writes
+                tc_fence_before_sync();    // ... and the TMEM stores
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ready0 + 8 * s);
             }
@@ -351,7 +425,10 @@ constexpr size_t smem_of(int bn) {
 
 int tc_bk(bool split3) { return split3 ? TcCfg<256, true>::BK : TcCfg<256, false>::BK; }
 int tc_stages(int bn, bool split3) { return split3 ? stages_of<true>(bn) : stages_of<false>(bn); }
-int tc_threads(bool split3) { return split3 ? TcCfg<256, true>::THREADS : TcCfg<256, false>::THREADS; }
+int tc_threads(int bn, bool split3) {
+    if (!split3) return TcCfg<256, false>::THREADS;
+    return bn == 64 ? TcCfg<64, true>::THREADS : (bn == 128 ? TcCfg<128, true>::THREADS : TcCfg<256, true>::THREADS);
+}
 size_t tc_smem_bytes(int bn, bool split3) { return split3 ? smem_of<true>(bn) : smem_of<false>(bn); }
 
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, bool split3,

@@ -131,11 +131,12 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
     x = plan(8192, 8192, 8192, "3xtf32")
     assert x["prep_a_name"] == "split" and x["prep_b_name"] == "split" and x["launches"] == 3
     assert x["workspace_bytes"] >= 4 * 8192 * 8192 * 4  # split parts (+ last-wave partials)
-    # narrow shapes (single-SM kernel): the kernel splits the operands itself in shared
-    # memory with four extra warps; no pre-pass, no operand workspace
+    # narrow shapes (single-SM kernel): the kernel splits the operands itself (A into
+    # tensor memory, B in shared memory) with one or two groups of four extra warps; no
+    # pre-pass, no operand workspace
     t = plan(8192, 64, 8192, "3xtf32")
     assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
-    assert t["threads"] == plan(8192, 64, 8192, "tf32")["threads"] + 128
+    assert t["threads"] - plan(8192, 64, 8192, "tf32")["threads"] in (128, 256)
     assert t["launches"] == 1 + (t["split_k"] > 1)
 
 
