@@ -68,6 +68,14 @@ namespace {
 #define PG_TC_XF_GROUPS 2
 #endif
 
+// K-blocks of BK per ring slot for the 64-wide tile (a compile-time tunable, 1 or
+// 2).  Its MMAs are short (48 cycles for 128 x 64 x 8), so the issuing thread's
+// per-slot work -- a barrier wait and one or two commits -- drains the tensor
+// pipe unless each slot carries more MMAs.
+#ifndef PG_TC_KPS
+#define PG_TC_KPS 2
+#endif
+
 template <int BN, bool SPLIT3>
 struct TcCfg {
     static constexpr int BM = kBM;
@@ -75,11 +83,17 @@ struct TcCfg {
     static constexpr int A_BYTES = BM * BK * 4;  // A tile of a slot
     static constexpr int B_BYTES = BN * BK * 4;  // B tile of a slot
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // FP32 tiles loaded per slot
-    // 3xTF32: B remainder slots, each with a TMEM stage of A's parts (4, 2 or 1
-    // for BN = 64, 128, 256, within 200 KiB of ring)
-    static constexpr int SMALL_STAGES = !SPLIT3 ? 0 : (BN == 256 ? 1 : (BN == 128 ? 2 : 4));
-    static constexpr int STAGES_RAW = (200 * 1024 - SMALL_STAGES * B_BYTES) / STAGE_BYTES;
+    static constexpr int KPS = BN == 64 ? PG_TC_KPS : 1;  // k-blocks per slot
+    static constexpr int SUB_BYTES = A_BYTES + B_BYTES;   // one k-block's FP32 tiles: [A][B]
+    static constexpr int STAGE_BYTES = KPS * SUB_BYTES;   // FP32 tiles loaded per slot
+    static constexpr int SMALL_BYTES = KPS * B_BYTES;     // B remainders of one slot
+    // 3xTF32: B remainder slots, each with a TMEM stage of A's parts (64 columns
+    // per k-block): 1, 2 or 4 slots for BN = 256, 128, 64 (2 with two k-blocks per
+    // slot), within 200 KiB of ring (224 KiB with two k-blocks per slot)
+    static constexpr int SMALL_STAGES =
+        !SPLIT3 ? 0 : (BN == 256 ? 1 : (BN == 128 ? 2 : (KPS == 2 ? 2 : 4)));
+    static constexpr int RING_BYTES = (KPS == 2 ? 224 : 200) * 1024;
+    static constexpr int STAGES_RAW = (RING_BYTES - SMALL_STAGES * SMALL_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     // 3xTF32 transform: groups of four warps (one per TMEM lane quarter), group g
     // taking k-blocks g, g + XF_GROUPS, ... so that one group's per-k-block
@@ -92,13 +106,16 @@ struct TcCfg {
     static constexpr int XF_WARPS = 4 * XF_GROUPS;      // transform warps
     static constexpr int THREADS = 192 + 32 * XF_WARPS;
     static constexpr int BAR_BYTES = (3 * STAGES + SMALL_STAGES + 1) * 8 + 16;
-    static constexpr size_t SMEM =
-        1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + static_cast<size_t>(SMALL_STAGES) * B_BYTES + BAR_BYTES;
+    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES +
+                                   static_cast<size_t>(SMALL_STAGES) * SMALL_BYTES + BAR_BYTES;
     // TMEM: the accumulator in columns [0, BN); with SPLIT3 the A operand stages
-    // at columns A_TMEM_COL + 64 j (big, then small), all 512 columns allocated
+    // at columns A_TMEM_COL + A_STAGE_COLS j, 64 per k-block (32 big, then 32
+    // small), all 512 columns allocated
     static constexpr uint32_t A_TMEM_COL = 256;
+    static constexpr uint32_t A_STAGE_COLS = 64 * KPS;
     static constexpr uint32_t TMEM_COLS = SPLIT3 ? 512 : BN;  // power of two >= 32
-    static_assert(!SPLIT3 || A_TMEM_COL + 64 * SMALL_STAGES <= 512, "TMEM operand stages");
+    static_assert(!SPLIT3 || A_TMEM_COL + A_STAGE_COLS * SMALL_STAGES <= 512, "TMEM operand stages");
+    static_assert(KPS == 1 || KPS == 2, "k-blocks per slot");
     static_assert(STAGES >= 2 && (STAGES >= 3 || !SPLIT3), "ring too shallow");
     static_assert(!SPLIT3 || (XF_GROUPS >= 1 && XF_GROUPS <= SMALL_STAGES && SMALL_STAGES <= STAGES),
                   "transform groups may run ahead of a barrier by at most one phase");
@@ -117,7 +134,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     uint8_t* smem = align_smem_1024(smem_raw);
     constexpr int SS = Cfg::SMALL_STAGES;
     uint8_t* small_ring = smem + S * Cfg::STAGE_BYTES;  // 3xTF32 B remainders, SS slots
-    uint64_t* bars = reinterpret_cast<uint64_t*>(small_ring + SS * Cfg::B_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(small_ring + SS * Cfg::SMALL_BYTES);
     // [0,S) full, [S,2S) empty, 2S accum, [2S+1, 3S+1) ready, [3S+1, 3S+1+SS) small_empty
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 1 + SS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -137,6 +154,8 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     const int slice = blockIdx.y;
     const int kb0 = slice * p.kb_per_split;
     const int nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
+    constexpr int KPS = Cfg::KPS;
+    const int nst = (nkb + KPS - 1) / KPS;  // ring slots' worth of k-blocks; the last may hold fewer
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -165,47 +184,50 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             prefetch_tmap(&tmB);
             int issued = 0;
             if (!(p.debug_flags & 1)) {
-                for (int it = 0; it < nkb; ++it) {
+                for (int it = 0; it < nst; ++it) {
                     const int s = it % S;
                     if (!mbar_wait_bounded(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                         raise_abort(abort_flag, p.status);
                         break;
                     }
                     const uint32_t full = full0 + 8 * s;
-                    mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
-                    const int32_t kc = (kb0 + it) * Cfg::BK;
-                    const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
-                    // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
-                    // box {32 rows, BK, 4 row groups} when m % 32 == 0, else four 2-D boxes
-                    // of 32 rows (both land as 4 x [BK][32] row groups).
-                    auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
-                        if (p.a_kmajor) {
-                            tma_load_2d(dst, map, kc, static_cast<int32_t>(m0), full);
-                        } else if (p.a3d) {
-                            tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(m0 / 32), full);
-                        } else {
+                    const int nsub = min(KPS, nkb - it * KPS);
+                    mbar_arrive_expect_tx(full, nsub * Cfg::SUB_BYTES);
+                    for (int u = 0; u < nsub; ++u) {
+                        const int32_t kc = (kb0 + it * KPS + u) * Cfg::BK;
+                        const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES);
+                        // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
+                        // box {32 rows, BK, 4 row groups} when m % 32 == 0, else four 2-D boxes
+                        // of 32 rows (both land as 4 x [BK][32] row groups).
+                        auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
+                            if (p.a_kmajor) {
+                                tma_load_2d(dst, map, kc, static_cast<int32_t>(m0), full);
+                            } else if (p.a3d) {
+                                tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(m0 / 32), full);
+                            } else {
 #pragma unroll
-                            for (int g = 0; g < 4; ++g)
-                                tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(m0 + 32 * g), kc,
-                                            full);
-                        }
-                    };
-                    // B K-major: one box of BN columns x BK.  B N-major (transb 'T'): BN/32
-                    // groups of 32 columns, as one 3-D box or as 2-D boxes.
-                    auto load_b = [&](uint32_t dst, const CUtensorMap* map) {
-                        if (!p.b_mnmajor) {
-                            tma_load_2d(dst, map, kc, static_cast<int32_t>(n0), full);
-                        } else if (p.b3d) {
-                            tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(n0 / 32), full);
-                        } else {
+                                for (int g = 0; g < 4; ++g)
+                                    tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(m0 + 32 * g), kc,
+                                                full);
+                            }
+                        };
+                        // B K-major: one box of BN columns x BK.  B N-major (transb 'T'): BN/32
+                        // groups of 32 columns, as one 3-D box or as 2-D boxes.
+                        auto load_b = [&](uint32_t dst, const CUtensorMap* map) {
+                            if (!p.b_mnmajor) {
+                                tma_load_2d(dst, map, kc, static_cast<int32_t>(n0), full);
+                            } else if (p.b3d) {
+                                tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(n0 / 32), full);
+                            } else {
 #pragma unroll
-                            for (int g = 0; g < BN / 32; ++g)
-                                tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(n0 + 32 * g), kc,
-                                            full);
-                        }
-                    };
-                    load_a(slot, &tmA);
-                    load_b(slot + Cfg::A_BYTES, &tmB);
+                                for (int g = 0; g < BN / 32; ++g)
+                                    tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(n0 + 32 * g), kc,
+                                                full);
+                            }
+                        };
+                        load_a(slot, &tmA);
+                        load_b(slot + Cfg::A_BYTES, &tmB);
+                    }
                     issued = it + 1;
                 }
             }
@@ -219,7 +241,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             uint32_t accumulate = 0;
             // A from TMEM (3xTF32) is K-major by construction
             const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !SPLIT3 && !p.a_kmajor, p.b_mnmajor != 0);
-            for (int it = 0; it < nkb; ++it) {
+            for (int it = 0; it < nst; ++it) {
                 const int s = it % S;
                 // 3xTF32: the transform warps have split the slot
                 if (!mbar_wait_bounded((SPLIT3 ? ready0 : full0) + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
@@ -227,26 +249,29 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
                 const int j = SS > 0 ? it % SS : 0;  // remainder slot and TMEM stage (3xTF32)
-                const uint32_t a_big = slot;
-                const uint32_t b_big = slot + Cfg::A_BYTES;
-                const uint32_t b_small = smem_u32(small_ring + j * Cfg::B_BYTES);
-                const uint32_t ta_big = tmem + Cfg::A_TMEM_COL + 64 * j;  // lane 0, A's big parts
+                const int nsub = min(KPS, nkb - it * KPS);
+                for (int u = 0; u < nsub; ++u) {
+                    const uint32_t a_big = smem_u32(smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES);
+                    const uint32_t b_big = a_big + Cfg::A_BYTES;
+                    const uint32_t b_small = smem_u32(small_ring + j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES);
+                    // lane 0, A's big parts of this k-block
+                    const uint32_t ta_big = tmem + Cfg::A_TMEM_COL + Cfg::A_STAGE_COLS * j + 64 * u;
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-                    const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
-                    if (SPLIT3) {
-                        const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
-                        const uint32_t tab = ta_big + 8 * kk;  // k-step kk: columns 8kk .. 8kk+7
-                        mma_tf32_tmem_a(tmem, tab + 32, bd, idesc, accumulate);  // small * big
-                        accumulate = 1;
-                        mma_tf32_tmem_a(tmem, tab, bsd, idesc, 1);  // big * small
-                        mma_tf32_tmem_a(tmem, tab, bd, idesc, 1);   // big * big
-                    } else {
-                        const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
-                        mma_tf32(tmem, ad, bd, idesc, accumulate);
-                        accumulate = 1;
+                    for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
+                        const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
+                        if (SPLIT3) {
+                            const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
+                            const uint32_t tab = ta_big + 8 * kk;  // k-step kk: columns 8kk .. 8kk+7
+                            mma_tf32_tmem_a(tmem, tab + 32, bd, idesc, accumulate);  // small * big
+                            accumulate = 1;
+                            mma_tf32_tmem_a(tmem, tab, bsd, idesc, 1);  // big * small
+                            mma_tf32_tmem_a(tmem, tab, bd, idesc, 1);   // big * big
+                        } else {
+                            const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
+                            mma_tf32(tmem, ad, bd, idesc, accumulate);
+                            accumulate = 1;
+                        }
                     }
                 }
                 mma_commit(empty0 + 8 * s);  // slot reusable once these MMAs have read it
@@ -261,14 +286,14 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             const int grp = (warp - 6) >> 2;
             const int t = threadIdx.x - 192 - 128 * grp;  // thread within the group
             const int q = warp & 3;  // TMEM lane quarter: A rows 32q .. 32q + 31
-            for (int it = grp; it < nkb; it += Cfg::XF_GROUPS) {
+            for (int it = grp; it < nst; it += Cfg::XF_GROUPS) {
                 const int s = it % S;
                 const int j = it % SS;
-                // The MMAs of k-block it - SS have released remainder slot j and its
-                // TMEM stage, then k-block it has landed.  A parity wait is exact only
+                // The MMAs of slot fill it - SS have released remainder slot j and its
+                // TMEM stage, then fill it has landed.  A parity wait is exact only
                 // while the awaited phase is the barrier's current or next one.  This
-                // group's previous k-block, it - XF_GROUPS >= it - SS, already saw the
-                // release of k-block it - XF_GROUPS - SS >= it - 2 SS, so small_empty[j]
+                // group's previous fill, it - XF_GROUPS >= it - SS, already saw the
+                // release of fill it - XF_GROUPS - SS >= it - 2 SS, so small_empty[j]
                 // is at most one phase behind.  MMAs complete in order, so once the
                 // MMAs of it - SS are done those of it - S <= it - SS are too, whose
                 // slot had landed before: full[s] is then at most one phase behind.
@@ -280,43 +305,47 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     if (lane == 0) raise_abort(abort_flag, p.status);
                     break;
                 }
-                uint8_t* slot = smem + s * Cfg::STAGE_BYTES;
-                // A row 32q + lane: its BK values.  K-major: 128-byte row in the
-                // 128-byte swizzle (16-byte chunk c at c ^ (row % 8)), read as float4s
-                // (the 8 rows of a quarter-warp hit 8 distinct chunk positions).
-                // M-major: row group q, BK lines of 32 rows, no swizzle.
-                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + Cfg::A_TMEM_COL + 64 * j;
+                const int nsub = min(KPS, nkb - it * KPS);
+                for (int u = 0; u < nsub; ++u) {
+                    uint8_t* slot = smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES;
+                    // A row 32q + lane: its BK values.  K-major: 128-byte row in the
+                    // 128-byte swizzle (16-byte chunk c at c ^ (row % 8)), read as float4s
+                    // (the 8 rows of a quarter-warp hit 8 distinct chunk positions).
+                    // M-major: row group q, BK lines of 32 rows, no swizzle.
+                    const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + Cfg::A_TMEM_COL +
+                                        Cfg::A_STAGE_COLS * j + 64 * u;
 #pragma unroll
-                for (int h = 0; h < Cfg::BK / 16; ++h) {  // 16 values of the row at a time
-                    float a[16];
-                    if (p.a_kmajor) {
-                        const uint32_t row = smem_u32(slot) + (32 * q + lane) * (Cfg::BK * 4);
+                    for (int h = 0; h < Cfg::BK / 16; ++h) {  // 16 values of the row at a time
+                        float a[16];
+                        if (p.a_kmajor) {
+                            const uint32_t row = smem_u32(slot) + (32 * q + lane) * (Cfg::BK * 4);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float4 v = lds128(row + (((4 * h + c) ^ (lane & 7)) << 4));
-                            a[4 * c] = v.x;
-                            a[4 * c + 1] = v.y;
-                            a[4 * c + 2] = v.z;
-                            a[4 * c + 3] = v.w;
+                            for (int c = 0; c < 4; ++c) {
+                                const float4 v = lds128(row + (((4 * h + c) ^ (lane & 7)) << 4));
+                                a[4 * c] = v.x;
+                                a[4 * c + 1] = v.y;
+                                a[4 * c + 2] = v.z;
+                                a[4 * c + 3] = v.w;
+                            }
+                        } else {
+                            const float* col = reinterpret_cast<const float*>(slot + q * Cfg::A_BOX_BYTES) + lane;
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) a[k] = col[32 * (16 * h + k)];
                         }
-                    } else {
-                        const float* col = reinterpret_cast<const float*>(slot + q * Cfg::A_BOX_BYTES) + lane;
+                        uint32_t big[16], sml[16];
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) a[k] = col[32 * (16 * h + k)];
+                        for (int k = 0; k < 16; ++k) {
+                            float b, r;
+                            split_tf32(a[k], b, r);
+                            big[k] = __float_as_uint(b);
+                            sml[k] = __float_as_uint(r);
+                        }
+                        tmem_st_32x32b_x16(ta + 16 * h, big);
+                        tmem_st_32x32b_x16(ta + 32 + 16 * h, sml);
                     }
-                    uint32_t big[16], sml[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float b, r;
-                        split_tf32(a[k], b, r);
-                        big[k] = __float_as_uint(b);
-                        sml[k] = __float_as_uint(r);
-                    }
-                    tmem_st_32x32b_x16(ta + 16 * h, big);
-                    tmem_st_32x32b_x16(ta + 32 + 16 * h, sml);
+                    split_tile_in_place<Cfg::B_BYTES, 128>(slot + Cfg::A_BYTES,
+                                                           small_ring + j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES, t);
                 }
-                split_tile_in_place<Cfg::B_BYTES, 128>(slot + Cfg::A_BYTES,
-                                                                      small_ring + j * Cfg::B_BYTES, t);
                 tmem_wait_st();
                 fence_proxy_async_smem();  // the tensor core reads the B writes
                 tc_fence_before_sync();    // ... and the TMEM stores
