@@ -241,34 +241,43 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             uint32_t accumulate = 0;
             // A from TMEM (3xTF32) is K-major by construction
             const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !SPLIT3 && !p.a_kmajor, p.b_mnmajor != 0);
+            // The 48-cycle MMAs of the 64-wide tile leave the issuing thread little
+            // time per instruction, so descriptors are not rebuilt per MMA: those of
+            // slot 0 are built once, and a slot, a k-block in it and a k-step only
+            // move the start address field (bits 0-13, in 16-byte units; shared
+            // addresses stay below 256 KiB, so the field does not overflow).
+            const bool a_k = p.a_kmajor != 0, b_k = p.b_mnmajor == 0;
+            const uint64_t a_desc0 = operand_desc<Cfg::BK>(smem_u32(smem), 0, a_k);
+            const uint64_t b_desc0 = operand_desc<Cfg::BK>(smem_u32(smem) + Cfg::A_BYTES, 0, b_k);
+            const uint64_t bs_desc0 = operand_desc<Cfg::BK>(smem_u32(small_ring), 0, b_k);
+            const uint32_t a_kstep = a_k ? 2 : 64, b_kstep = b_k ? 2 : 64;  // 32 B or 1 KiB per k-step
+            int s = 0, j = 0;  // ring slot, remainder slot and TMEM stage (3xTF32)
+            uint32_t phase = 0;
             for (int it = 0; it < nst; ++it) {
-                const int s = it % S;
                 // 3xTF32: the transform warps have split the slot
-                if (!mbar_wait_bounded((SPLIT3 ? ready0 : full0) + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
+                if (!mbar_wait_bounded((SPLIT3 ? ready0 : full0) + 8 * s, phase, p.timeout_ns, abort_flag)) {
                     raise_abort(abort_flag, p.status);
                     break;
                 }
                 tc_fence_after_sync();
-                const int j = SS > 0 ? it % SS : 0;  // remainder slot and TMEM stage (3xTF32)
                 const int nsub = min(KPS, nkb - it * KPS);
                 for (int u = 0; u < nsub; ++u) {
-                    const uint32_t a_big = smem_u32(smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES);
-                    const uint32_t b_big = a_big + Cfg::A_BYTES;
-                    const uint32_t b_small = smem_u32(small_ring + j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES);
+                    const uint32_t off = static_cast<uint32_t>(s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES) >> 4;
+                    const uint32_t soff = static_cast<uint32_t>(j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES) >> 4;
                     // lane 0, A's big parts of this k-block
                     const uint32_t ta_big = tmem + Cfg::A_TMEM_COL + Cfg::A_STAGE_COLS * j + 64 * u;
 #pragma unroll
                     for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-                        const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
+                        const uint64_t bd = b_desc0 + (off + kk * b_kstep);
                         if (SPLIT3) {
-                            const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
+                            const uint64_t bsd = bs_desc0 + (soff + kk * b_kstep);
                             const uint32_t tab = ta_big + 8 * kk;  // k-step kk: columns 8kk .. 8kk+7
                             mma_tf32_tmem_a(tmem, tab + 32, bd, idesc, accumulate);  // small * big
                             accumulate = 1;
                             mma_tf32_tmem_a(tmem, tab, bsd, idesc, 1);  // big * small
                             mma_tf32_tmem_a(tmem, tab, bd, idesc, 1);   // big * big
                         } else {
-                            const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
+                            const uint64_t ad = a_desc0 + (off + kk * a_kstep);
                             mma_tf32(tmem, ad, bd, idesc, accumulate);
                             accumulate = 1;
                         }
@@ -276,6 +285,11 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                 }
                 mma_commit(empty0 + 8 * s);  // slot reusable once these MMAs have read it
                 if (SPLIT3) mma_commit(small_empty0 + 8 * j);  // and so is the remainder slot
+                if (++s == S) {
+                    s = 0;
+                    phase ^= 1;
+                }
+                if (SS > 0 && ++j == SS) j = 0;
             }
             mma_commit(accum_bar);  // accumulator complete (also after an abort)
         }
