@@ -316,9 +316,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
     } else if (warp == 1) {
         // ---------------- MMA issuer (CTA 0 of the pair) ----------------
         if (leader && lane == 0) {
-            int it = 0, lu = 0;
+            int lu = 0;
             bool ok = true;
             const uint32_t idesc = idesc_tf32(2 * Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
+            // Descriptors of slot 0's tiles, built once; a slot and a k-step only move
+            // the start address field (bits 0-13, in 16-byte units; shared addresses
+            // stay below 256 KiB, so the field does not overflow).
+            const bool a_k = p.a_kmajor != 0, b_k = p.b_mnmajor == 0;
+            const uint32_t slot0 = smem_u32(smem);
+            const uint64_t a_desc0 = operand_desc<Cfg::BK>(slot0, 0, a_k);
+            const uint64_t as_desc0 = operand_desc<Cfg::BK>(slot0 + Cfg::A_BYTES, 0, a_k);
+            const uint64_t b_desc0 = operand_desc<Cfg::BK>(slot0 + Cfg::OPS * Cfg::A_BYTES, 0, b_k);
+            const uint64_t bs_desc0 = operand_desc<Cfg::BK>(slot0 + Cfg::OPS * Cfg::A_BYTES + Cfg::B_BYTES, 0, b_k);
+            const uint32_t a_kstep = a_k ? 2 : 64, b_kstep = b_k ? 2 : 64;  // 32 B or 1 KiB per k-step
+            int s = 0;  // ring slot
+            uint32_t phase = 0;
             for (int u = pair; u < units && ok; u += pairs, ++lu) {
                 int64_t m0, n0;
                 int slice, kb0, nkb, t;
@@ -331,26 +343,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                 tc_fence_after_sync();
                 const uint32_t d = tmem + buf * BN;
                 uint32_t accumulate = 0;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!mbar_wait_bounded(full0 + 8 * s, (it / S) & 1, p.timeout_ns, abort_flag)) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait_bounded(full0 + 8 * s, phase, p.timeout_ns, abort_flag)) {
                         raise_abort(abort_flag, p.status);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
-                    const uint32_t a_big = slot;
-                    const uint32_t a_small = slot + Cfg::A_BYTES;
-                    const uint32_t b_big = slot + Cfg::OPS * Cfg::A_BYTES;
-                    const uint32_t b_small = b_big + Cfg::B_BYTES;
+                    const uint32_t off = static_cast<uint32_t>(s * Cfg::STAGE_BYTES) >> 4;
 #pragma unroll
                     for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-                        const uint64_t ad = operand_desc<Cfg::BK>(a_big, kk, p.a_kmajor != 0);
-                        const uint64_t bd = operand_desc<Cfg::BK>(b_big, kk, p.b_mnmajor == 0);
+                        const uint64_t ad = a_desc0 + (off + kk * a_kstep);
+                        const uint64_t bd = b_desc0 + (off + kk * b_kstep);
                         if (SPLIT3) {
-                            const uint64_t asd = operand_desc<Cfg::BK>(a_small, kk, p.a_kmajor != 0);
-                            const uint64_t bsd = operand_desc<Cfg::BK>(b_small, kk, p.b_mnmajor == 0);
+                            const uint64_t asd = as_desc0 + (off + kk * a_kstep);
+                            const uint64_t bsd = bs_desc0 + (off + kk * b_kstep);
                             mma_tf32_pair(d, asd, bd, idesc, accumulate);
                             accumulate = 1;
                             mma_tf32_pair(d, ad, bsd, idesc, 1);
@@ -361,6 +368,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                         }
                     }
                     mma_commit_pair(empty0 + 8 * s);  // both CTAs' slot s reusable after these MMAs
+                    if (++s == S) {
+                        s = 0;
+                        phase ^= 1;
+                    }
                 }
                 if (ok) mma_commit_pair(acc_full0 + 8 * buf);  // unit's accumulator complete
             }
