@@ -90,13 +90,24 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // Block -> (tile, K slice).  With the last-wave split, blocks from tail_first
+    // on take the last partial wave's tiles, tail_split K slices each.
+    int tile = blockIdx.x, slice = blockIdx.y, kb0, nkb;
+    const bool tail = p.tail_split > 1 && tile >= p.tail_first;
+    if (tail) {
+        const int v = tile - p.tail_first;
+        tile = p.tail_first + v / p.tail_split;
+        slice = v % p.tail_split;
+        kb0 = slice * p.tail_kb;
+        nkb = min(kb0 + p.tail_kb, p.kb_total) - kb0;
+    } else {
+        kb0 = slice * p.kb_per_split;
+        nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
+    }
     int tile_m, tile_n;
-    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
+    tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
     const int64_t m0 = static_cast<int64_t>(tile_m) * Cfg::BM;
     const int64_t n0 = static_cast<int64_t>(tile_n) * BN;
-    const int slice = blockIdx.y;
-    const int kb0 = slice * p.kb_per_split;
-    const int nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -197,6 +208,53 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
             mbar_wait_bounded(full0 + 8 * (it % S), (it / S) & 1, p.timeout_ns, nullptr);
     }
     if (!ok || *abort_flag) return;
+
+    // ---------------- last-wave fix-up ----------------
+    // A tail slice stores its partial block ([column][row], BM x BN floats), and
+    // each warp counts itself in for the outputs it holds (a warp of every slice
+    // holds the same ones); the warp that arrives last adds the blocks in slice
+    // order (0, 1, ...: the same association whichever slice is last, so the
+    // result is deterministic) and runs the epilogue below on the sum.  No
+    // block-wide barrier: a warp that gave up on a wait has already returned.
+    if (tail) {
+        const int tt = tile - p.tail_first;
+        float* part0 = p.tail_P + static_cast<int64_t>(tt) * p.tail_split * (Cfg::BM * BN);
+#pragma unroll
+        for (int jj = 0; jj < JJ; ++jj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float* d = part0 + static_cast<int64_t>(slice) * (Cfg::BM * BN) + (tn + Cfg::TGN * jj) * Cfg::BM +
+                           64 * h + 4 * tm;
+                *reinterpret_cast<float4*>(d) =
+                    make_float4(acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y);
+            }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.tail_cnt + tt * Cfg::CWARPS + warp, 1) == p.tail_split - 1;
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence();
+#pragma unroll
+        for (int jj = 0; jj < JJ; ++jj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t off = (tn + Cfg::TGN * jj) * Cfg::BM + 64 * h + 4 * tm;
+                const float4 own =
+                    make_float4(acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y);
+                float4 sum = slice == 0 ? own : __ldcg(reinterpret_cast<const float4*>(part0 + off));
+                for (int sl = 1; sl < p.tail_split; ++sl) {
+                    const float4 v = sl == slice ? own
+                                                 : __ldcg(reinterpret_cast<const float4*>(
+                                                       part0 + static_cast<int64_t>(sl) * (Cfg::BM * BN) + off));
+                    sum.x += v.x;
+                    sum.y += v.y;
+                    sum.z += v.z;
+                    sum.w += v.w;
+                }
+                acc[2 * h][jj] = make_float2(sum.x, sum.y);
+                acc[2 * h + 1][jj] = make_float2(sum.z, sum.w);
+            }
+    }
 
     // ---------------- epilogue ----------------
     // C is read ahead of the stores, G columns of the thread's tile at a time:

@@ -109,7 +109,8 @@ size_t tail_bytes(const sgemm_plan_t& pl) {
     return region(static_cast<int64_t>(pl.tail_tiles) * pl.tail_split * pl.bm * pl.bn);
 }
 size_t tail_counter_bytes(const sgemm_plan_t& pl) {
-    return region(static_cast<int64_t>(pl.tail_tiles) * 2 * tc2_epilogue_warps());
+    const int per_tile = pl.kernel == SGEMM_KERNEL_TC2 ? 2 * tc2_epilogue_warps() : pl.threads / 32;
+    return region(static_cast<int64_t>(pl.tail_tiles) * per_tile);
 }
 
 // The planner.  Pure host arithmetic: no device is touched.  allow_tail = false
@@ -222,10 +223,11 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->split_k = static_cast<int>(split);
     pl->k_blocks_per_split = static_cast<int>(per);
 
-    // Last-wave split (SM pairs): when the tiles fill whole waves of pairs and a
+    // Last-wave split (SM pairs, and FFMA): when the tiles fill whole waves and a
     // last wave at most half full, cut each last-wave tile's K into s slices (at
-    // least 8 K blocks each, s <= 4) so the last wave keeps every pair busy.
-    if (pair && split == 1 && g_force_split.load() == 0 && allow_tail) {
+    // least 8 K blocks each, s <= 4) so the last wave keeps every pair (every
+    // FFMA CTA slot) busy.
+    if ((pair || !tc) && split == 1 && g_force_split.load() == 0 && allow_tail) {
         const int64_t waves = tiles / capacity, rem = tiles % capacity;
         if (waves >= 1 && rem > 0 && 2 * rem <= capacity) {
             const int64_t s = std::min<int64_t>({capacity / rem, 4, pl->k_blocks / 8});
@@ -402,7 +404,9 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
     cudaError_t e;
     CUtensorMap tmA, tmB;
     if (pl.kernel == SGEMM_KERNEL_FFMA) {
-        const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
+        // one block per tile and K slice; the last wave's tiles take tail_split blocks each
+        const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n + pl.tail_tiles * (pl.tail_split - 1)),
+                        static_cast<unsigned>(pl.split_k));
         if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
         if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
         if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");

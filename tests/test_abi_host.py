@@ -149,12 +149,17 @@ def test_plan_last_wave_split(lib):
     q = plan(8192, 8192, 8192, "3xtf32")
     assert q["tail_tiles"] == 1024 - 13 * 76 and q["tail_split"] == 2
     # no split when the tiles fill whole waves, the last wave is over half full,
-    # K is short, or the problem already uses split-K; FFMA tiles are not split
+    # K is short, or the problem already uses split-K
     assert plan(256 * 19, 256 * 8, 4096, "tf32")["tail_split"] == 1          # 152 tiles = 2 waves
     assert plan(256 * 10, 256 * 12, 4096, "tf32")["tail_split"] == 1         # 120 tiles: 44 > 76/2
     assert plan(4096, 4096, 96, "tf32")["tail_split"] == 1                  # 3 K blocks
     assert plan(512, 512, 8192, "tf32")["tail_split"] == 1                  # split-K instead
-    assert plan(8192, 8192, 8192, "ffma")["tail_split"] == 1
+    # FFMA: 4096 tiles of 128x128 over 152 SMs x 2 CTA slots = 13 waves + 144 tiles;
+    # the 144 last-wave tiles run as 2 K slices (288 blocks), in the same launch
+    f = plan(8192, 8192, 8192, "ffma")
+    assert f["tail_tiles"] == 4096 - 13 * 304 and f["tail_split"] == 2 and f["launches"] == 1
+    assert f["workspace_bytes"] >= 144 * 2 * 128 * 128 * 4
+    assert plan(16384, 16384, 16384, "ffma")["tail_split"] == 1  # 272-tile last wave: over half full
 
 
 def test_plan_skinny_k_uses_deterministic_split(lib):

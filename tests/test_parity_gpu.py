@@ -200,6 +200,25 @@ def test_last_wave_split(mode, mnk):
     assert H.padding_intact(p, out1, C)
 
 
+@pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4100, 2500, 600)])
+def test_last_wave_split_ffma(mnk):
+    """FFMA: the last partial wave's 128x128 tiles run as 2-4 K slices; the warp of the
+    last slice to finish sums the partial blocks in slice order -- ragged edges, beta != 0,
+    bitwise repeatable."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, ldc=m + 3, alpha=-1.25, beta=0.5, dist="normal", seed=47)
+    plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "ffma")
+    assert plan["kernel_name"] == "ffma" and plan["tail_split"] > 1, plan
+    A, B, C = synth.make(p)
+    out1, ok1 = H.run_gpu(p, "ffma", A, B, C)
+    out2, ok2 = H.run_gpu(p, "ffma", A, B, C)
+    assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, out1), cref, den, oracle.TOL["ffma"])
+    assert res["ok"], res
+    assert H.padding_intact(p, out1, C)
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
                                  (128, 256, 32), (257, 513, 1031), (64, 64, 200000), (160, 200, 300), (288, 130, 77),
