@@ -70,14 +70,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// Arrive without release semantics: for signals that publish no memory writes.
-// The epilogue frees a TMEM accumulator buffer with it once tcgen05.wait::ld has
-// returned (the buffer is no longer read); a release arrive would first wait
-// for all of the warp's outstanding stores of C to be performed.
+// Arrive on a barrier of another CTA of the cluster, without release semantics:
+// for signals that publish no memory writes.  The epilogue frees a TMEM
+// accumulator buffer with it once tcgen05.wait::ld has returned (the buffer is
+// no longer read); a release arrive would first wait for all of the warp's
+// outstanding stores of C to be performed.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
