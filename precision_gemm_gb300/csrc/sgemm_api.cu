@@ -139,15 +139,23 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // SM measured fastest) and the narrowest of 128/256 covering n for tcgen05 --
     // except that a tensor-core product whose 128 x 64 tiles fit in one wave of
     // SMs runs on those (single-SM kernel) when it is 3xTF32 (which there splits
-    // in shared memory instead of running two pre-passes over A and B) or a TF32
-    // product under 4 GFLOP (lowest latency up to ~1024^3; with long K the SM
-    // pairs and a K split stream A faster).
+    // on chip instead of running two pre-passes over A and B) or a TF32 product
+    // under 4 GFLOP (lowest latency up to ~1024^3; with long K the SM pairs and a
+    // K split stream A faster).
     // Tiny FFMA products (under 2 GFLOP, their 128 x 64 tiles filling at most half
     // the SMs) take the 64-wide tile too, with thinner K slices below: more CTAs
     // share the few k-blocks.
     int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
     const int64_t tiles64 = cdiv(m, kBM) * cdiv(n, 64);
     if (tc && tiles64 <= std::max(num_sms, 1) && (split3 || 2.0 * m * n * k <= 4e9)) bn = 64;
+    // One row of tiles (m <= 128) whose 128-wide tiles fit in one wave: 128-wide
+    // tiles on single SMs, for 3xTF32 (128 x 128 x 8 MMAs run at the full rate,
+    // 128 x 64 x 8 ones at two thirds, and each issue carries twice the work:
+    // 128 x 4096 x 8192 0.099 -> 0.071 ms, 128 x 128 x 262144 0.087 -> 0.065) and
+    // for TF32 above 4 GFLOP (as fast as 256-wide tiles or faster: 128 x 4096 x
+    // 8192 0.044 -> 0.040 ms).
+    if (tc && m <= kBM && n > 64 && cdiv(n, 128) <= std::max(num_sms, 1) && (split3 || 2.0 * m * n * k > 4e9))
+        bn = 128;
     const bool tiny_ffma = !tc && 2 * tiles64 <= std::max(num_sms, 1) && 2.0 * m * n * k <= 2e9;
     if (tiny_ffma) bn = 64;
     const int fbn = g_force_bn.load();

@@ -182,7 +182,15 @@ def test_plan_pair_kernel_only_above_128_rows(lib):
     assert small["split_k"] == 152 // 32
     long_k = plan(512, 512, 65536, "tf32")                             # long K: SM pairs, 2 x 2 tiles, split K
     assert long_k["kernel_name"] == "tc2" and long_k["split_k"] == 76 // 4
-    # 3xTF32 keeps the single-SM kernel at any K (its split in shared memory avoids two pre-passes)
+    # one row of tiles (m <= 128): 128-wide single-SM tiles for 3xTF32 and for TF32 above 4 GFLOP
+    for mnk in ((128, 128, 262144), (128, 4096, 8192), (100, 3000, 2000), (64, 8192, 8192)):
+        q = plan(*mnk, "3xtf32")
+        assert q["kernel_name"] == "tc" and q["bn"] == 128, (mnk, q)
+    assert plan(128, 4096, 8192, "tf32")["bn"] == 128
+    assert plan(100, 3000, 2000, "tf32")["bn"] == 64                  # 1.2 GFLOP: the 64-wide rule
+    assert plan(128, 64, 262144, "3xtf32")["bn"] == 64                 # n <= 64
+    assert plan(128, 65536, 4096, "tf32")["bn"] == 256                 # 512 tiles of 128: over one wave
+    # 3xTF32 keeps the single-SM kernel at any K (its on-chip split avoids two pre-passes)
     assert plan(8192, 128, 8192, "3xtf32")["kernel_name"] == "tc"
     assert plan(8192, 128, 8192, "tf32")["kernel_name"] == "tc2"
     assert plan(1024, 1024, 1024, "3xtf32")["kernel_name"] == "tc"     # 128 tiles: one wave
