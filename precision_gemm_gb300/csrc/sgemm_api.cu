@@ -147,23 +147,31 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // share the few k-blocks.
     int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
     const int64_t tiles64 = cdiv(m, kBM) * cdiv(n, 64);
-    if (tc && tiles64 <= std::max(num_sms, 1) && (split3 || 2.0 * m * n * k <= 4e9)) bn = 64;
-    // One row of tiles (m <= 128) whose 128-wide tiles fit in one wave: 128-wide
-    // tiles on single SMs, for 3xTF32 (128 x 128 x 8 MMAs run at the full rate,
-    // 128 x 64 x 8 ones at two thirds, and each issue carries twice the work:
-    // 128 x 4096 x 8192 0.099 -> 0.071 ms, 128 x 128 x 262144 0.087 -> 0.065) and
-    // for TF32 above 4 GFLOP (as fast as 256-wide tiles or faster: 128 x 4096 x
-    // 8192 0.044 -> 0.040 ms).
-    if (tc && m <= kBM && n > 64 && cdiv(n, 128) <= std::max(num_sms, 1) && (split3 || 2.0 * m * n * k > 4e9))
-        bn = 128;
+    const bool one_wave64 = tc && tiles64 <= std::max(num_sms, 1);
+    if (one_wave64 && (split3 || 2.0 * m * n * k <= 4e9)) bn = 64;
+    // 128-wide tiles on single SMs (128 x 128 x 8 MMAs run at the full rate,
+    // 128 x 64 x 8 ones at two thirds, and each issue carries twice the work):
+    //  - one row of tiles (m <= 128) whose 128-wide tiles fit in one wave, for
+    //    3xTF32 and for TF32 above 4 GFLOP: 3xTF32 128 x 4096 x 8192 0.099 ->
+    //    0.071 ms, 128 x 128 x 262144 0.087 -> 0.065; TF32 128 x 4096 x 8192
+    //    0.044 -> 0.040 (256-wide tiles before);
+    //  - 3xTF32 whose 64-wide tiles fit in one wave and whose K is long (>= 2048):
+    //    4096 x 128 x 8192 0.098 -> 0.070 ms, 512 x 256 x 32768 0.087 -> 0.062;
+    //    with short K the halved tile count costs more (1024^3 0.031 -> 0.034).
+    const bool single128 =
+        tc && n > 64 &&
+        ((m <= kBM && cdiv(n, 128) <= std::max(num_sms, 1) && (split3 || 2.0 * m * n * k > 4e9)) ||
+         (split3 && one_wave64 && k >= 2048));
+    if (single128) bn = 128;
     const bool tiny_ffma = !tc && 2 * tiles64 <= std::max(num_sms, 1) && 2.0 * m * n * k <= 2e9;
     if (tiny_ffma) bn = 64;
     const int fbn = g_force_bn.load();
     if (fbn) bn = fbn;
     pl->bn = bn;
     // Tensor-core modes run on SM pairs (256-row tiles, cta_group::2) when m > 128;
-    // a single-SM 128-row tile serves m <= 128 and the 64-wide tile.
-    const bool pair = tc && m > kBM && bn >= 128;
+    // a single-SM 128-row tile serves m <= 128, the 64-wide tile and the 128-wide
+    // tiles chosen above.
+    const bool pair = tc && m > kBM && bn >= 128 && !(single128 && fbn == 0);
 
     // Operand preparation: TMA needs a 16-byte aligned base and a leading
     // dimension that is a multiple of 16 bytes.  The tensor-core kernels read
