@@ -180,7 +180,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // A M-major and B K-major only, so a transposed operand is copied transposed.
     // 3xTF32 on SM pairs reads operands split by a pre-pass (the large shapes, where
     // the pre-pass is cheap next to the product); the single-SM kernel splits them
-    // itself in shared memory (the narrow shapes, where a pre-pass would dominate).
+    // itself on chip (the narrow shapes, where a pre-pass would dominate).
     const bool a_ok = aligned16(A) && (lda % 4 == 0);
     const bool b_ok = aligned16(B) && (ldb % 4 == 0);
     if (split3 && pair) {
