@@ -220,7 +220,7 @@ def test_plan_transposed_operands(lib):
     # 3xTF32 on SM pairs splits them without transposing: ld is the stored row count rounded to 4
     x = plan(3000, 2000, 101, "3xtf32", transa="T", transb="T")
     assert x["kernel_name"] == "tc2" and x["prep_a_name"] == "split" and x["ld_a"] == 104 and x["ld_b"] == 2000
-    # the single-SM kernel reads them in place and splits in shared memory; a stored
+    # the single-SM kernel reads them in place and splits them on chip; a stored
     # row count that is not a multiple of 4 still needs a plain copy, ld rounded up
     y = plan(100, 64, 101, "3xtf32", transa="T", transb="T")
     assert y["kernel_name"] == "tc" and y["prep_a_name"] == "copy" and y["ld_a"] == 104
