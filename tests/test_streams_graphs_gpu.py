@@ -120,7 +120,7 @@ def test_host_async_calls_overlap_and_match_sync(same_stream):
     assert pg.device_status() == 0
 
 
-@pytest.mark.parametrize("mode", ("tf32", "3xtf32"))
+@pytest.mark.parametrize("mode", ("ffma", "tf32", "3xtf32"))
 def test_captured_last_wave_split_replays(mode):
     """A product that splits its last wave along K (arrival counters zeroed by a
     memset before the kernel) captured into a graph: every replay starts from
