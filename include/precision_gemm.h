@@ -224,9 +224,10 @@ uint64_t sgemm_set_wait_timeout(uint64_t ns);
 
 /*
  * sgemm_force_plan -- tuning override for later calls from any thread:
- * bn in {0, 64, 128, 256} fixes the CTA tile width, split_k > 0 fixes the number
- * of K slices (clamped to the number of K blocks).  0 restores the automatic
- * choice.  Returns -1 for an unsupported bn, -2 for a negative split_k.
+ * bn in {0, 64, 128, 256, 512} fixes the CTA tile width (512 exists for TF32 on
+ * SM pairs only and means 256 elsewhere), split_k > 0 fixes the number of K
+ * slices (clamped to the number of K blocks).  0 restores the automatic choice.
+ * Returns -1 for an unsupported bn, -2 for a negative split_k.
  */
 int sgemm_force_plan(int bn, int split_k);
 

@@ -165,8 +165,17 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     if (single128) bn = 128;
     const bool tiny_ffma = !tc && 2 * tiles64 <= std::max(num_sms, 1) && 2.0 * m * n * k <= 2e9;
     if (tiny_ffma) bn = 64;
+    // TF32 on SM pairs: 256 x 512 tiles (two N = 256 MMAs per k-step) need 48 B/clk
+    // per SM of operand feed at the full MMA rate against 64 for 256 x 256 tiles
+    // (bulk copies sustain ~65 per SM), at the price of a single TMEM accumulator
+    // (the epilogue of a tile no longer overlaps the next tile's MMAs).  Faster
+    // with K >= 4096 and at least two waves of tiles: 8192^3 897 -> 964 TFLOP/s,
+    // 6144^3 875 -> 936, 16384 x 4096 x 8192 889 -> 959; at K = 2048 1 % slower.
+    if (tc && !split3 && m > kBM && bn == 256 && k >= 4096 &&
+        cdiv(m, 2 * kBM) * cdiv(n, 512) >= 2 * std::max(num_sms / 2, 1))
+        bn = 512;
     const int fbn = g_force_bn.load();
-    if (fbn) bn = fbn;
+    if (fbn) bn = (fbn == 512 && (!tc || split3 || m <= kBM)) ? 256 : fbn;  // 512: TF32 on SM pairs only
     pl->bn = bn;
     // Tensor-core modes run on SM pairs (256-row tiles, cta_group::2) when m > 128;
     // a single-SM 128-row tile serves m <= 128, the 64-wide tile and the 128-wide
@@ -430,7 +439,8 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
         // tcgen05: A in 32-row boxes (M-major, 32-byte-atom swizzle), B in boxes of
         // pl.bk x (bn, or bn/2 per CTA on SM pairs).
         const bool pair = pl.kernel == SGEMM_KERNEL_TC2;
-        const uint32_t b_cols = pair ? pl.bn / 2 : pl.bn;
+        // (the 512-wide pair tile stages each CTA's B columns as two halves of 128)
+        const uint32_t b_cols = pair ? (pl.bn == 512 ? 128 : pl.bn / 2) : pl.bn;
         // K-major operands: rows of BK floats, 128- or 64-byte swizzle.  M/N-major
         // operands: groups of 32 rows in the 32-byte-atom 128-byte swizzle, as one
         // 3-D box when the extent is a multiple of 32, else as 2-D boxes.
@@ -951,7 +961,8 @@ PG_EXPORT int sgemm_device_status(void* stream, int clear) {
 PG_EXPORT uint64_t sgemm_set_wait_timeout(uint64_t ns) { return g_timeout_ns.exchange(ns); }
 
 PG_EXPORT int sgemm_force_plan(int bn, int split_k) {
-    if (!(bn == 0 || bn == 64 || bn == 128 || bn == 256)) return fail(-1, "bn %d is not 0, 64, 128 or 256", bn);
+    if (!(bn == 0 || bn == 64 || bn == 128 || bn == 256 || bn == 512))
+        return fail(-1, "bn %d is not 0, 64, 128, 256 or 512", bn);
     if (split_k < 0) return fail(-2, "split_k %d is negative", split_k);
     g_force_bn = bn;
     g_force_split = split_k;

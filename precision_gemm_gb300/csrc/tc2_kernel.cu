@@ -151,8 +151,15 @@ struct Tc2Cfg {
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES;
-    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulator buffers
-    static_assert(BN == 128 || BN == 256, "BN");
+    // Accumulator buffers in TMEM: two (epilogue of one unit overlaps the MMAs of
+    // the next) up to BN = 256; the 512-wide tile takes all 512 columns, one buffer.
+    static constexpr int NBUF = BN == 512 ? 1 : 2;
+    static constexpr uint32_t TMEM_COLS = NBUF * BN;
+    // MMAs per k-step: one of N = BN, or two of N = 256 for the 512-wide tile (each
+    // CTA then stages its B columns as two halves of 128, one per MMA)
+    static constexpr int NMMA = BN == 512 ? 2 : 1;
+    static constexpr int MMA_N = BN / NMMA;
+    static_assert(BN == 128 || BN == 256 || (BN == 512 && !SPLIT3), "BN");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "slots need 1 KiB alignment");
     static_assert(STAGES >= 3, "ring too shallow");
 };
@@ -283,7 +290,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                         }
                     };
                     auto load_b = [&](uint32_t dst, const CUtensorMap* map) {
-                        if (!p.b_mnmajor) {
+                        if (Cfg::NMMA == 2) {
+                            // two halves of 128 columns: n0 + 256 j + 128 rank + [0, 128)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const int32_t nj = static_cast<int32_t>(n0) + 256 * j + 128 * static_cast<int32_t>(rank);
+                                const uint32_t dj = dst + j * (Cfg::B_BYTES / 2);
+                                if (!p.b_mnmajor) {
+                                    tma_load_2d_pair(dj, map, kc, nj, bar);
+                                } else if (p.b3d) {
+                                    tma_load_3d_pair(dj, map, 0, kc, nj / 32, bar);
+                                } else {
+#pragma unroll
+                                    for (int g = 0; g < 4; ++g)
+                                        tma_load_2d_pair(dj + g * Cfg::A_BOX_BYTES, map, nj + 32 * g, kc, bar);
+                                }
+                            }
+                        } else if (!p.b_mnmajor) {
                             tma_load_2d_pair(dst, map, kc, nb, bar);
                         } else if (p.b3d) {
                             tma_load_3d_pair(dst, map, 0, kc, nb / 32, bar);
@@ -315,7 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
         if (leader && lane == 0) {
             int lu = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_tf32(2 * Cfg::BM, BN, !p.a_kmajor, p.b_mnmajor != 0);
+            const uint32_t idesc = idesc_tf32(2 * Cfg::BM, Cfg::MMA_N, !p.a_kmajor, p.b_mnmajor != 0);
             // Descriptors of slot 0's tiles, built once; a slot and a k-step only move
             // the start address field (bits 0-13, in 16-byte units; shared addresses
             // stay below 256 KiB, so the field does not overflow).
@@ -332,8 +355,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                 int64_t m0, n0;
                 int slice, kb0, nkb, t;
                 unit_geometry(u, m0, n0, slice, kb0, nkb, t);
-                const int buf = lu & 1;
-                if (!mbar_wait_bounded(acc_empty0 + 8 * buf, ((lu >> 1) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                const int buf = lu % Cfg::NBUF;
+                if (!mbar_wait_bounded(acc_empty0 + 8 * buf, ((lu / Cfg::NBUF) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                     raise_abort(abort_flag, p.status);
                     break;
                 }
@@ -360,7 +383,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                             mma_tf32_pair(d, ad, bsd, idesc, 1);
                             mma_tf32_pair(d, ad, bd, idesc, 1);
                         } else {
-                            mma_tf32_pair(d, ad, bd, idesc, accumulate);
+#pragma unroll
+                            for (int j = 0; j < Cfg::NMMA; ++j)  // B half j: 128 rows = 16 KiB further
+                                mma_tf32_pair(d + j * Cfg::MMA_N, ad, bd + j * 1024, idesc, accumulate);
                             accumulate = 1;
                         }
                     }
@@ -394,9 +419,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
             float* tpart = tail ? p.tail_P + (static_cast<int64_t>(tile - p.tail_first) * p.tail_split + slice) *
                                                  (2 * Cfg::BM) * BN
                                 : nullptr;
-            const int buf = lu & 1;
+            const int buf = lu % Cfg::NBUF;
             const bool ready = __all_sync(
-                0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * buf, (lu >> 1) & 1, p.timeout_ns, abort_flag));
+                0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * buf, (lu / Cfg::NBUF) & 1, p.timeout_ns, abort_flag));
             if (!ready) {
                 if (lane == 0) raise_abort(abort_flag, p.status);
                 break;
@@ -582,11 +607,13 @@ int tc2_epilogue_warps() { return Tc2Cfg<256, false>::EPI_WARPS; }
 
 int tc2_stages(int bn, bool split3) {
     if (split3) return bn == 128 ? Tc2Cfg<128, true>::STAGES : Tc2Cfg<256, true>::STAGES;
+    if (bn == 512) return Tc2Cfg<512, false>::STAGES;
     return bn == 128 ? Tc2Cfg<128, false>::STAGES : Tc2Cfg<256, false>::STAGES;
 }
 
 size_t tc2_smem_bytes(int bn, bool split3) {
     if (split3) return bn == 128 ? Tc2Cfg<128, true>::SMEM : Tc2Cfg<256, true>::SMEM;
+    if (bn == 512) return Tc2Cfg<512, false>::SMEM;
     return bn == 128 ? Tc2Cfg<128, false>::SMEM : Tc2Cfg<256, false>::SMEM;
 }
 
@@ -599,6 +626,8 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmAs, const CU
     if (bn == 256)
         return split3 ? Launcher<256, true>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched)
                       : Launcher<256, false>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched);
+    if (bn == 512 && !split3)
+        return Launcher<512, false>::run(tmA, tmAs, tmB, tmBs, p, units, num_sms, stream, pairs_launched);
     return cudaErrorInvalidValue;
 }
 

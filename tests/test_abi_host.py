@@ -120,8 +120,9 @@ def plan(m, n, k, mode="ffma", transa="N", transb="N", lda=None, ldb=None, ldc=N
 def test_plan_square_uses_wide_tiles_and_no_split(lib):
     for mode in ("ffma", "tf32", "3xtf32"):
         p = plan(8192, 8192, 8192, mode)
-        # FFMA: 128 x 128 tiles, two CTAs per SM; tensor cores: 256 x 256 tiles on SM pairs
-        bm, bn = (128, 128) if mode == "ffma" else (256, 256)
+        # FFMA: 128 x 128 tiles, two CTAs per SM; tensor cores on SM pairs: 256 x 512 tiles
+        # for TF32 (long K, two waves or more of tiles), 256 x 256 for 3xTF32
+        bm, bn = {"ffma": (128, 128), "tf32": (256, 512), "3xtf32": (256, 256)}[mode]
         assert p["bn"] == bn and p["bm"] == bm and p["split_k"] == 1
         assert p["tiles_m"] == 8192 // bm and p["tiles_n"] == 8192 // bn
         assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc2")
@@ -138,6 +139,24 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
     assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
     assert t["threads"] - plan(8192, 64, 8192, "tf32")["threads"] in (128, 256)
     assert t["launches"] == 1 + (t["split_k"] > 1)
+
+
+def test_plan_tf32_512_wide_pair_tiles(lib):
+    assert plan(6144, 6144, 6144, "tf32")["bn"] == 512
+    assert plan(16384, 4096, 8192, "tf32")["bn"] == 512
+    assert plan(8192, 8192, 2048, "tf32")["bn"] == 256       # K < 4096: the overlapped epilogue wins
+    assert plan(4096, 4096, 16384, "tf32")["bn"] == 256      # 128 tiles of 256 x 512: under two waves
+    assert plan(8192, 8192, 8192, "3xtf32")["bn"] == 256     # 3xTF32 keeps 256 x 256
+    assert plan(16384, 16384, 64, "tf32")["bn"] == 256       # skinny K
+    # forcing 512 where it does not exist means 256
+    pg.force_plan(512, 0)
+    try:
+        assert plan(8192, 8192, 8192, "3xtf32")["bn"] == 256
+        assert plan(8192, 8192, 8192, "ffma")["bn"] == 256
+        assert plan(100, 8192, 8192, "tf32")["bn"] == 256
+        assert plan(2000, 3000, 700, "tf32")["bn"] == 512
+    finally:
+        pg.force_plan(0, 0)
 
 
 def test_plan_last_wave_split(lib):

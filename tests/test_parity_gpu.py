@@ -200,6 +200,27 @@ def test_last_wave_split(mode, mnk):
     assert H.padding_intact(p, out1, C)
 
 
+@pytest.mark.parametrize("mnk,tb", [((3000, 1700, 777), "N"), ((2048, 1536, 512), "T"), ((700, 2600, 1300), "N"),
+                                    ((1000, 1100, 300), "T"), ((5000, 1900, 600), "N")])
+def test_pair_kernel_512_tiles(mnk, tb):
+    """TF32 on SM pairs with 256x512 tiles (two N = 256 MMAs per k-step, one TMEM
+    accumulator of 512 columns, each CTA's B columns staged as two halves of 128):
+    ragged edges, N-major B as 3-D and as 2-D boxes, beta != 0, and a last-wave split
+    (5000 x 1900: 80 tiles on 76 pairs)."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, transb=tb, ldc=m + 3, alpha=1.25, beta=-0.5, dist="normal", seed=59)
+    pg.load_library()
+    try:
+        pg.force_plan(512, 0)
+        plan = pg.sgemm_plan("N", tb, m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "tf32")
+        assert plan["kernel_name"] == "tc2" and plan["bn"] == 512, plan
+        if m == 5000:
+            assert plan["tail_split"] > 1, plan
+        _assert_ok(H.check_problem(p, "tf32"), "512 %s %s" % (mnk, tb))
+    finally:
+        pg.force_plan(0, 0)
+
+
 @pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4100, 2500, 600)])
 def test_last_wave_split_ffma(mnk):
     """FFMA: the last partial wave's 128x128 tiles run as 2-4 K slices; the warp of the
