@@ -234,18 +234,17 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
         if (lane == 0) last = atomicAdd(p.tail_cnt + tt * Cfg::CWARPS + warp, 1) == p.tail_split - 1;
         if (!__shfl_sync(0xffffffffu, last, 0)) return;
         __threadfence();
+        // All slices' blocks, this one's included, are read back from L2 (the
+        // thread's own stores are ordered before its loads), so the accumulators
+        // need not stay live beside the sums.
 #pragma unroll
         for (int jj = 0; jj < JJ; ++jj)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int64_t off = (tn + Cfg::TGN * jj) * Cfg::BM + 64 * h + 4 * tm;
-                const float4 own =
-                    make_float4(acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y);
-                float4 sum = slice == 0 ? own : __ldcg(reinterpret_cast<const float4*>(part0 + off));
+                const float* src = part0 + (tn + Cfg::TGN * jj) * Cfg::BM + 64 * h + 4 * tm;
+                float4 sum = __ldcg(reinterpret_cast<const float4*>(src));
                 for (int sl = 1; sl < p.tail_split; ++sl) {
-                    const float4 v = sl == slice ? own
-                                                 : __ldcg(reinterpret_cast<const float4*>(
-                                                       part0 + static_cast<int64_t>(sl) * (Cfg::BM * BN) + off));
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + sl * (Cfg::BM * BN)));
                     sum.x += v.x;
                     sum.y += v.y;
                     sum.z += v.z;
