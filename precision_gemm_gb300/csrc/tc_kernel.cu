@@ -380,32 +380,38 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             const bool row_ok = i < p.m;
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
             const float alpha = p.alpha, beta = p.beta;
+            // Chunks of EC columns: 32, or 16 in 3xTF32, whose extra warps leave 128
+            // registers a thread (two 32-value arrays would spill).
+            constexpr int EC = SPLIT3 ? 16 : 32;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int64_t jb = n0 + 32 * c;
+            for (int c = 0; c < BN / EC; ++c) {
+                const int64_t jb = n0 + EC * c;
                 if (jb >= p.n) break;  // uniform across the warp
-                const int jn = (p.n - jb < 32) ? static_cast<int>(p.n - jb) : 32;
-                // All 32 loads of C are issued before the tensor-memory read and
+                const int jn = (p.n - jb < EC) ? static_cast<int>(p.n - jb) : EC;
+                // All EC loads of C are issued before the tensor-memory read and
                 // before any store: interleaved with the stores, each load would wait
                 // for the previous store (the compiler cannot rule out that they
                 // alias) and the epilogue would run at DRAM latency.
                 float* dst = p.C + jb * p.ldc + i;
                 const bool read_c = row_ok && p.split == 1 && beta != 0.0f;
-                float cv[32];
+                float cv[EC];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(lane_base + 32 * c, v);
+                for (int t = 0; t < EC; ++t) cv[t] = (read_c && t < jn) ? dst[t * p.ldc] : 0.0f;
+                uint32_t v[EC];
+                if constexpr (EC == 32)
+                    tmem_ld_32x32b_x32(lane_base + EC * c, v);
+                else
+                    tmem_ld_32x32b_x16(lane_base + EC * c, v);
                 tmem_wait_ld();
                 if (!row_ok) continue;
                 if (p.split > 1) {
                     float* part = p.P + slice * p.p_stride + jb * p.ldp + i;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t)
+                    for (int t = 0; t < EC; ++t)
                         if (t < jn) part[t * p.ldp] = __uint_as_float(v[t]);
                 } else {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) {
+                    for (int t = 0; t < EC; ++t) {
                         if (t < jn) {
                             float o = alpha * __uint_as_float(v[t]);
                             if (beta != 0.0f) o = fmaf(beta, cv[t], o);
