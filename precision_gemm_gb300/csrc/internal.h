@@ -32,6 +32,7 @@ struct GemmParams {
     int32_t a_kmajor;        // tcgen05 kernels: A is read K-major (transa = 'T'), else M-major
     int32_t b_mnmajor;       // tcgen05 kernels: B is read N-major (transb = 'T'), else K-major
     int32_t b3d;             // tcgen05 kernels, N-major B: tensor map 3-D {32, k, n/32}
+    int32_t b_presplit;      // single-SM 3xTF32, BN <= 128: B's TF32 parts come split (tmB big, tmBs small)
     // Last-wave split (SM-pair kernel, split == 1): tiles [tail_first, tiles) each
     // run as tail_split K slices of tail_kb blocks; every slice stores its partial
     // 256 x BN block in tail_P ([tail tile][slice][column][row]), and per epilogue
@@ -67,8 +68,9 @@ int tc_bk(bool split3);
 int tc_stages(int bn, bool split3);
 int tc_threads(int bn, bool split3);
 size_t tc_smem_bytes(int bn, bool split3);
-cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, bool split3,
-                      dim3 grid, cudaStream_t stream);
+// tmBs: B's remainders when p.b_presplit (otherwise unused; pass tmB).
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
+                      int bn, bool split3, dim3 grid, cudaStream_t stream);
 
 // tcgen05 kernel on SM pairs (cta_group::2, persistent, double-buffered TMEM):
 // pair tile 256 x bn, bn in {128, 256}; launches min(units, resident pairs) pairs.

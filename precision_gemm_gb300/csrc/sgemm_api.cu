@@ -190,14 +190,21 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // 3xTF32 on SM pairs reads operands split by a pre-pass (the large shapes, where
     // the pre-pass is cheap next to the product); the single-SM kernel splits them
     // itself on chip (the narrow shapes, where a pre-pass would dominate).
+    // The single-SM kernel's on-chip split of B is repeated by every row of tiles
+    // that shares B; from four rows of tiles and K >= 4096 on, a pre-pass splits B
+    // once and TMA brings both parts (64- and 128-wide tiles, whose sub-slots keep
+    // room for B's remainders): 3xTF32 8192 x 64 x 8192 0.0925 -> 0.0870 ms,
+    // 8192 x 128 x 8192 0.121 -> 0.103; with short K the pre-pass launch costs more
+    // than it saves (1024^3 0.027 -> 0.033).
     const bool a_ok = aligned16(A) && (lda % 4 == 0);
     const bool b_ok = aligned16(B) && (ldb % 4 == 0);
+    const bool presplit_b = split3 && !pair && bn <= 128 && cdiv(m, kBM) >= 4 && k >= 4096;
     if (split3 && pair) {
         pl->prep_a = SGEMM_PREP_SPLIT;
         pl->prep_b = SGEMM_PREP_SPLIT;
     } else if (tc) {
         pl->prep_a = a_ok ? SGEMM_PREP_NONE : SGEMM_PREP_COPY;
-        pl->prep_b = b_ok ? SGEMM_PREP_NONE : SGEMM_PREP_COPY;
+        pl->prep_b = presplit_b ? SGEMM_PREP_SPLIT : (b_ok ? SGEMM_PREP_NONE : SGEMM_PREP_COPY);
     } else {
         pl->prep_a = (a_ok && is_notrans(transa)) ? SGEMM_PREP_NONE
                                                   : (is_notrans(transa) ? SGEMM_PREP_COPY : SGEMM_PREP_TRANSPOSE);
@@ -264,9 +271,9 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     }
 
     size_t ws = 0;
-    const int parts = (split3 && pair) ? 2 : 1;
-    if (pl->prep_a != SGEMM_PREP_NONE) ws += parts * region(pl->ld_a * (rows_a == m ? k : m));
-    if (pl->prep_b != SGEMM_PREP_NONE) ws += parts * region(pl->ld_b * (rows_b == k ? n : k));
+    const int parts_a = pl->prep_a == SGEMM_PREP_SPLIT ? 2 : 1, parts_b = pl->prep_b == SGEMM_PREP_SPLIT ? 2 : 1;
+    if (pl->prep_a != SGEMM_PREP_NONE) ws += parts_a * region(pl->ld_a * (rows_a == m ? k : m));
+    if (pl->prep_b != SGEMM_PREP_NONE) ws += parts_b * region(pl->ld_b * (rows_b == k ? n : k));
     if (split > 1) ws += region(split * round_up(m, 4) * n);
     if (pl->tail_split > 1) ws += tail_bytes(*pl) + tail_counter_bytes(*pl);
     pl->workspace_bytes = ws;
@@ -479,8 +486,12 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
             if ((e = launch_tc2(tmA, tmAs, tmB, tmBs, gp, pl.bn, split3, units, num_sms, st, &pairs)) != cudaSuccess)
                 return fail_cuda(e, "tcgen05 SM-pair GEMM kernel");
         } else {
+            // 3xTF32 with B split by the pre-pass: remainders through tmBs
+            CUtensorMap tmBs = tmB;
+            gp.b_presplit = (split3 && b_small != nullptr) ? 1 : 0;
+            if (gp.b_presplit && (rc = encode_b(&tmBs, b_small))) return rc;
             const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
-            if ((e = launch_tc(tmA, tmB, gp, pl.bn, split3, grid, st)) != cudaSuccess)
+            if ((e = launch_tc(tmA, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
                 return fail_cuda(e, "tcgen05 GEMM kernel");
         }
     }

@@ -40,13 +40,19 @@
 //      reads the row's BK values and writes big and small with tcgen05.st into a
 //      TMEM operand stage (lane = row, one value per column: big in 32 columns,
 //      small in the next 32), from which the MMAs read A;
-//   B  split in place in the slot, remainders at the same offset of a slot of a
-//      second, short ring of B remainders.
+//   B  split in place in the slot; for BN <= 128 the remainders go to the space
+//      the sub-slot keeps free right in front of B (layout [A][B small][B]), for
+//      BN = 256 to a slot of a second, short ring of B remainders.
 // They then fence their writes for the tensor core and arrive on the slot's
-// "ready" barrier, which the MMA thread waits for.  Per k-step it issues
-// small*big, big*small, big*big into the same accumulator (the small*small term
-// is below FP32 resolution and dropped), then releases the slot and the
-// remainder slot with its TMEM stage.  3xTF32 thus reads each operand byte from
+// "ready" barrier, which the MMA thread waits for.  Per k-step it issues, for
+// BN <= 128, big * [small | big] as one MMA of N = 2 BN into accumulator
+// columns [0, 2 BN) and small * big into columns [BN, 2 BN) -- two MMAs where
+// three would do the same products, and the 64-wide tile's N = 128 MMA runs at
+// the full rate where N = 64 runs at two thirds of it; the epilogue adds the
+// two halves.  For BN = 256 it issues small*big, big*small, big*big into one
+// accumulator.  (The small*small term is below FP32 resolution and dropped.)
+// It then releases the slot and the remainder slot with its TMEM stage.
+// 3xTF32 thus reads each operand byte from
 // DRAM once, like TF32 (these shapes are HBM-bound), and A's parts never pass
 // through shared memory (a split in place for A as well, the earlier form of
 // this kernel, measured 3-7 % slower on the narrow shapes).  Two groups of
@@ -84,16 +90,25 @@ struct TcCfg {
     static constexpr int B_BYTES = BN * BK * 4;  // B tile of a slot
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
     static constexpr int KPS = BN == 64 ? PG_TC_KPS : 1;  // k-blocks per slot
-    static constexpr int SUB_BYTES = A_BYTES + B_BYTES;   // one k-block's FP32 tiles: [A][B]
-    static constexpr int STAGE_BYTES = KPS * SUB_BYTES;   // FP32 tiles loaded per slot
-    static constexpr int SMALL_BYTES = KPS * B_BYTES;     // B remainders of one slot
-    // 3xTF32: B remainder slots, each with a TMEM stage of A's parts (64 columns
-    // per k-block): 1, 2 or 4 slots for BN = 256, 128, 64 (2 with two k-blocks per
-    // slot), within 200 KiB of ring (224 KiB with two k-blocks per slot)
+    // 3xTF32 with BN <= 128 ("fused"): a k-block's sub-slot is [A][B small][B],
+    // the B remainders written by the transform warps right in front of the
+    // split B, so that one N = 2 BN operand covers both.  BN = 256 keeps its
+    // remainders in a second, short ring.
+    static constexpr bool FUSED = SPLIT3 && BN <= 128;
+    static constexpr int B_OFF = A_BYTES + (FUSED ? B_BYTES : 0);   // B in a sub-slot
+    static constexpr int SUB_BYTES = B_OFF + B_BYTES;               // one k-block's sub-slot
+    static constexpr int LOAD_BYTES = A_BYTES + B_BYTES;            // what TMA brings per k-block
+    static constexpr int STAGE_BYTES = KPS * SUB_BYTES;             // one ring slot
+    static constexpr int SMALL_BYTES = KPS * B_BYTES;               // B remainders of one slot
+    // 3xTF32: remainder slots, each with a TMEM stage of A's parts (64 columns
+    // per k-block): 1, 2 or 4 for BN = 256, 128, 64 (2 with two k-blocks per
+    // slot); only BN = 256 also holds B remainders in them.  Within 200 KiB of
+    // ring (224 KiB with two k-blocks per slot).
     static constexpr int SMALL_STAGES =
         !SPLIT3 ? 0 : (BN == 256 ? 1 : (BN == 128 ? 2 : (KPS == 2 ? 2 : 4)));
+    static constexpr int SMALL_RING_BYTES = FUSED ? 0 : SMALL_STAGES * SMALL_BYTES;
     static constexpr int RING_BYTES = (KPS == 2 ? 224 : 200) * 1024;
-    static constexpr int STAGES_RAW = (RING_BYTES - SMALL_STAGES * SMALL_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_RAW = (RING_BYTES - SMALL_RING_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     // 3xTF32 transform: groups of four warps (one per TMEM lane quarter), group g
     // taking k-blocks g, g + XF_GROUPS, ... so that one group's per-k-block
@@ -107,14 +122,18 @@ struct TcCfg {
     static constexpr int THREADS = 192 + 32 * XF_WARPS;
     static constexpr int BAR_BYTES = (3 * STAGES + SMALL_STAGES + 1) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES +
-                                   static_cast<size_t>(SMALL_STAGES) * SMALL_BYTES + BAR_BYTES;
-    // TMEM: the accumulator in columns [0, BN); with SPLIT3 the A operand stages
-    // at columns A_TMEM_COL + A_STAGE_COLS j, 64 per k-block (32 big, then 32
-    // small), all 512 columns allocated
+                                   static_cast<size_t>(SMALL_RING_BYTES) + BAR_BYTES;
+    // TMEM: the accumulator in columns [0, BN) (fused 3xTF32: [0, 2 BN), the
+    // big * small products in the first BN and big * big + small * big in the
+    // second); with SPLIT3 the A operand stages at columns A_TMEM_COL +
+    // A_STAGE_COLS j, 64 per k-block (32 big, then 32 small), all 512 columns
+    // allocated
+    static constexpr int ACC_COLS = FUSED ? 2 * BN : BN;
     static constexpr uint32_t A_TMEM_COL = 256;
     static constexpr uint32_t A_STAGE_COLS = 64 * KPS;
     static constexpr uint32_t TMEM_COLS = SPLIT3 ? 512 : BN;  // power of two >= 32
     static_assert(!SPLIT3 || A_TMEM_COL + A_STAGE_COLS * SMALL_STAGES <= 512, "TMEM operand stages");
+    static_assert(!SPLIT3 || ACC_COLS <= static_cast<int>(A_TMEM_COL), "accumulator below the operand stages");
     static_assert(KPS == 1 || KPS == 2, "k-blocks per slot");
     static_assert(STAGES >= 2 && (STAGES >= 3 || !SPLIT3), "ring too shallow");
     static_assert(!SPLIT3 || (XF_GROUPS >= 1 && XF_GROUPS <= SMALL_STAGES && SMALL_STAGES <= STAGES),
@@ -127,14 +146,14 @@ struct TcCfg {
 template <int BN, bool SPLIT3>
 __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmBs, const GemmParams p) {
     using Cfg = TcCfg<BN, SPLIT3>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
     constexpr int SS = Cfg::SMALL_STAGES;
-    uint8_t* small_ring = smem + S * Cfg::STAGE_BYTES;  // 3xTF32 B remainders, SS slots
-    uint64_t* bars = reinterpret_cast<uint64_t*>(small_ring + SS * Cfg::SMALL_BYTES);
+    uint8_t* small_ring = smem + S * Cfg::STAGE_BYTES;  // 3xTF32 with BN = 256: B remainders, SS slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(small_ring + Cfg::SMALL_RING_BYTES);
     // [0,S) full, [S,2S) empty, 2S accum, [2S+1, 3S+1) ready, [3S+1, 3S+1+SS) small_empty
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 1 + SS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -156,6 +175,9 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     const int nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
     constexpr int KPS = Cfg::KPS;
     const int nst = (nkb + KPS - 1) / KPS;  // ring slots' worth of k-blocks; the last may hold fewer
+    // B arrives split (big through tmB, remainders through tmBs into the space in
+    // front of B): the transform warps split A only.
+    const bool b_presplit = Cfg::FUSED && p.b_presplit != 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -182,6 +204,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
         if (lane == 0) {
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
+            if (b_presplit) prefetch_tmap(&tmBs);
             int issued = 0;
             if (!(p.debug_flags & 1)) {
                 for (int it = 0; it < nst; ++it) {
@@ -192,7 +215,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     }
                     const uint32_t full = full0 + 8 * s;
                     const int nsub = min(KPS, nkb - it * KPS);
-                    mbar_arrive_expect_tx(full, nsub * Cfg::SUB_BYTES);
+                    mbar_arrive_expect_tx(full, nsub * (Cfg::LOAD_BYTES + (b_presplit ? Cfg::B_BYTES : 0)));
                     for (int u = 0; u < nsub; ++u) {
                         const int32_t kc = (kb0 + it * KPS + u) * Cfg::BK;
                         const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES);
@@ -226,7 +249,8 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                             }
                         };
                         load_a(slot, &tmA);
-                        load_b(slot + Cfg::A_BYTES, &tmB);
+                        load_b(slot + Cfg::B_OFF, &tmB);
+                        if (b_presplit) load_b(slot + Cfg::A_BYTES, &tmBs);
                     }
                     issued = it + 1;
                 }
@@ -241,6 +265,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             uint32_t accumulate = 0;
             // A from TMEM (3xTF32) is K-major by construction
             const uint32_t idesc = idesc_tf32(Cfg::BM, BN, !SPLIT3 && !p.a_kmajor, p.b_mnmajor != 0);
+            const uint32_t idesc2 = idesc_tf32(Cfg::BM, 2 * BN, false, p.b_mnmajor != 0);  // fused: N = 2 BN
             // The 48-cycle MMAs of the 64-wide tile leave the issuing thread little
             // time per instruction, so descriptors are not rebuilt per MMA: those of
             // slot 0 are built once, and a slot, a k-block in it and a k-step only
@@ -248,8 +273,10 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             // addresses stay below 256 KiB, so the field does not overflow).
             const bool a_k = p.a_kmajor != 0, b_k = p.b_mnmajor == 0;
             const uint64_t a_desc0 = operand_desc<Cfg::BK>(smem_u32(smem), 0, a_k);
-            const uint64_t b_desc0 = operand_desc<Cfg::BK>(smem_u32(smem) + Cfg::A_BYTES, 0, b_k);
-            const uint64_t bs_desc0 = operand_desc<Cfg::BK>(smem_u32(small_ring), 0, b_k);
+            const uint64_t b_desc0 = operand_desc<Cfg::BK>(smem_u32(smem) + Cfg::B_OFF, 0, b_k);
+            // B remainders: in front of B in the sub-slot (fused), else in the second ring
+            const uint64_t bs_desc0 =
+                operand_desc<Cfg::BK>(Cfg::FUSED ? smem_u32(smem) + Cfg::A_BYTES : smem_u32(small_ring), 0, b_k);
             const uint32_t a_kstep = a_k ? 2 : 64, b_kstep = b_k ? 2 : 64;  // 32 B or 1 KiB per k-step
             int s = 0, j = 0;  // ring slot, remainder slot and TMEM stage (3xTF32)
             uint32_t phase = 0;
@@ -263,13 +290,22 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                 const int nsub = min(KPS, nkb - it * KPS);
                 for (int u = 0; u < nsub; ++u) {
                     const uint32_t off = static_cast<uint32_t>(s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES) >> 4;
-                    const uint32_t soff = static_cast<uint32_t>(j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES) >> 4;
+                    const uint32_t soff =
+                        Cfg::FUSED ? off : static_cast<uint32_t>(j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES) >> 4;
                     // lane 0, A's big parts of this k-block
                     const uint32_t ta_big = tmem + Cfg::A_TMEM_COL + Cfg::A_STAGE_COLS * j + 64 * u;
 #pragma unroll
                     for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
                         const uint64_t bd = b_desc0 + (off + kk * b_kstep);
-                        if (SPLIT3) {
+                        if (Cfg::FUSED) {
+                            // big * [small | big] into columns [0, 2 BN), then small * big
+                            // into [BN, 2 BN): two MMAs per k-step instead of three
+                            const uint64_t bsd = bs_desc0 + (soff + kk * b_kstep);
+                            const uint32_t tab = ta_big + 8 * kk;  // k-step kk: columns 8kk .. 8kk+7
+                            mma_tf32_tmem_a(tmem, tab, bsd, idesc2, accumulate);
+                            accumulate = 1;
+                            mma_tf32_tmem_a(tmem + BN, tab + 32, bd, idesc, 1);
+                        } else if (SPLIT3) {
                             const uint64_t bsd = bs_desc0 + (soff + kk * b_kstep);
                             const uint32_t tab = ta_big + 8 * kk;  // k-step kk: columns 8kk .. 8kk+7
                             mma_tf32_tmem_a(tmem, tab + 32, bd, idesc, accumulate);  // small * big
@@ -357,8 +393,11 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                         tmem_st_32x32b_x16(ta + 16 * h, big);
                         tmem_st_32x32b_x16(ta + 32 + 16 * h, sml);
                     }
-                    split_tile_in_place<Cfg::B_BYTES, 128>(slot + Cfg::A_BYTES,
-                                                           small_ring + j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES, t);
+                    if (!b_presplit)
+                        split_tile_in_place<Cfg::B_BYTES, 128>(
+                            slot + Cfg::B_OFF,
+                            Cfg::FUSED ? slot + Cfg::A_BYTES : small_ring + j * Cfg::SMALL_BYTES + u * Cfg::B_BYTES,
+                            t);
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();  // the tensor core reads the B writes
@@ -402,6 +441,14 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     tmem_ld_32x32b_x32(lane_base + EC * c, v);
                 else
                     tmem_ld_32x32b_x16(lane_base + EC * c, v);
+                if constexpr (Cfg::FUSED) {
+                    // the two partial accumulators: big * small, and big * big + small * big
+                    uint32_t w[EC];
+                    tmem_ld_32x32b_x16(lane_base + BN + EC * c, w);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < EC; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(w[t]));
+                }
                 tmem_wait_ld();
                 if (!row_ok) continue;
                 if (p.split > 1) {
@@ -437,24 +484,24 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
 }
 
 template <int BN, bool SPLIT3>
-cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, dim3 grid,
-                        cudaStream_t stream) {
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
+                        dim3 grid, cudaStream_t stream) {
     using Cfg = TcCfg<BN, SPLIT3>;
     auto kern = tc_gemm_kernel<BN, SPLIT3>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, p);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, tmBs, p);
     return cudaGetLastError();
 }
 
 template <bool SPLIT3>
-cudaError_t launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, dim3 grid,
-                      cudaStream_t st) {
+cudaError_t launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bs, const GemmParams& p,
+                      dim3 grid, cudaStream_t st) {
     switch (bn) {
-        case 64: return launch_impl<64, SPLIT3>(a, b, p, grid, st);
-        case 128: return launch_impl<128, SPLIT3>(a, b, p, grid, st);
-        case 256: return launch_impl<256, SPLIT3>(a, b, p, grid, st);
+        case 64: return launch_impl<64, SPLIT3>(a, b, bs, p, grid, st);
+        case 128: return launch_impl<128, SPLIT3>(a, b, bs, p, grid, st);
+        case 256: return launch_impl<256, SPLIT3>(a, b, bs, p, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -480,9 +527,11 @@ int tc_threads(int bn, bool split3) {
 }
 size_t tc_smem_bytes(int bn, bool split3) { return split3 ? smem_of<true>(bn) : smem_of<false>(bn); }
 
-cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, bool split3,
-                      dim3 grid, cudaStream_t stream) {
-    return split3 ? launch_bn<true>(bn, tmA, tmB, p, grid, stream) : launch_bn<false>(bn, tmA, tmB, p, grid, stream);
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
+                      int bn, bool split3, dim3 grid, cudaStream_t stream) {
+    if (p.b_presplit && !(split3 && bn <= 128)) return cudaErrorInvalidValue;  // pre-split B: fused 3xTF32 only
+    return split3 ? launch_bn<true>(bn, tmA, tmB, tmBs, p, grid, stream)
+                  : launch_bn<false>(bn, tmA, tmB, tmBs, p, grid, stream);
 }
 
 }  // namespace pg

@@ -132,13 +132,21 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
     x = plan(8192, 8192, 8192, "3xtf32")
     assert x["prep_a_name"] == "split" and x["prep_b_name"] == "split" and x["launches"] == 3
     assert x["workspace_bytes"] >= 4 * 8192 * 8192 * 4  # split parts (+ last-wave partials)
-    # narrow shapes (single-SM kernel): the kernel splits the operands itself (A into
-    # tensor memory, B in shared memory) with one or two groups of four extra warps; no
-    # pre-pass, no operand workspace
+    # narrow shapes (single-SM kernel): the kernel splits A itself (into tensor memory)
+    # with one or two groups of four extra warps; B is split on chip too, except with
+    # K >= 4096 and four or more rows of tiles sharing B, where a pre-pass splits it once
     t = plan(8192, 64, 8192, "3xtf32")
-    assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "none"
+    assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "split"
     assert t["threads"] - plan(8192, 64, 8192, "tf32")["threads"] in (128, 256)
-    assert t["launches"] == 1 + (t["split_k"] > 1)
+    assert t["launches"] == 2 + (t["split_k"] > 1)
+    assert t["workspace_bytes"] >= 2 * 64 * 8192 * 4
+    w = plan(128, 4096, 8192, "3xtf32")
+    assert w["kernel_name"] == "tc" and w["prep_a_name"] == "none" and w["prep_b_name"] == "none"
+    assert w["launches"] == 1 + (w["split_k"] > 1)
+    assert plan(384, 64, 8192, "3xtf32")["prep_b_name"] == "none"    # three rows of tiles
+    assert plan(512, 64, 8192, "3xtf32")["prep_b_name"] == "split"   # four
+    assert plan(8192, 64, 8192, "tf32")["prep_b_name"] == "none"     # TF32 reads B as stored
+    assert plan(1024, 1024, 1024, "3xtf32")["prep_b_name"] == "none"  # short K: the pre-pass costs more
 
 
 def test_plan_tf32_512_wide_pair_tiles(lib):

@@ -221,6 +221,29 @@ def test_pair_kernel_512_tiles(mnk, tb):
         pg.force_plan(0, 0)
 
 
+@pytest.mark.parametrize("mnk,tb,ld_pad,beta", [((2000, 64, 4100), "N", 1, -0.5), ((1100, 100, 5000), "T", 0, 0.75),
+                                                 ((4096, 128, 4096), "N", 2, 0.0), ((600, 40, 4500), "T", 3, 1.0)])
+def test_single_sm_3xtf32_presplit_b(mnk, tb, ld_pad, beta):
+    """3xTF32 on single SMs with B split by a pre-pass (four or more rows of tiles share
+    B, K >= 4096): TMA brings B's remainders into the room in front of B and one
+    N = 2 BN MMA takes big * [small | big]; ragged m, n and K, N-major B as 2-D boxes
+    (n % 32 != 0), unaligned leading dimensions, beta 0 and not; bitwise repeatable."""
+    m, n, k = mnk
+    lda = m + ld_pad
+    ldb = (k if tb == "N" else n) + ld_pad
+    p = synth.Problem(m, n, k, transb=tb, lda=lda, ldb=ldb, ldc=m + 3, alpha=1.5, beta=beta, dist="normal", seed=61)
+    plan = pg.sgemm_plan("N", tb, m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "3xtf32")
+    assert plan["kernel_name"] == "tc" and plan["prep_b_name"] == "split" and plan["bn"] <= 128, plan
+    A, B, C = synth.make(p)
+    out1, ok1 = H.run_gpu(p, "3xtf32", A, B, C)
+    out2, ok2 = H.run_gpu(p, "3xtf32", A, B, C)
+    assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, out1), cref, den, oracle.TOL["3xtf32"])
+    assert res["ok"], res
+    assert H.padding_intact(p, out1, C)
+
+
 @pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4100, 2500, 600)])
 def test_last_wave_split_ffma(mnk):
     """FFMA: the last partial wave's 128x128 tiles run as 2-4 K slices; the warp of the
