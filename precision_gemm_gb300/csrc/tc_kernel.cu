@@ -74,10 +74,13 @@ namespace {
 #define PG_TC_XF_GROUPS 2
 #endif
 
-// K-blocks of BK per ring slot for the 64-wide tile (a compile-time tunable, 1 or
-// 2).  Its MMAs are short (48 cycles for 128 x 64 x 8), so the issuing thread's
-// per-slot work -- a barrier wait and one or two commits -- drains the tensor
-// pipe unless each slot carries more MMAs.
+// K-blocks of BK per ring slot for the 64-wide TF32 tile (a compile-time
+// tunable, 1 or 2).  Its MMAs are short (48 cycles for 128 x 64 x 8), so the
+// issuing thread's per-slot work -- a barrier wait and a commit -- drains the
+// tensor pipe unless each slot carries more MMAs.  The fused 3xTF32 form issues
+// 112 cycles of MMAs per k-step and does better with one k-block per slot, which
+// leaves room for seven slots and six TMEM operand stages (8192 x 64 x 8192:
+// 0.087 -> 0.083 ms against two k-blocks per slot with three of each).
 #ifndef PG_TC_KPS
 #define PG_TC_KPS 2
 #endif
@@ -89,7 +92,7 @@ struct TcCfg {
     static constexpr int A_BYTES = BM * BK * 4;  // A tile of a slot
     static constexpr int B_BYTES = BN * BK * 4;  // B tile of a slot
     static constexpr int A_BOX_BYTES = 32 * BK * 4;
-    static constexpr int KPS = BN == 64 ? PG_TC_KPS : 1;  // k-blocks per slot
+    static constexpr int KPS = (BN == 64 && !SPLIT3) ? PG_TC_KPS : 1;  // k-blocks per slot
     // 3xTF32 with BN <= 128 ("fused"): a k-block's sub-slot is [A][B small][B],
     // the B remainders written by the transform warps right in front of the
     // split B, so that one N = 2 BN operand covers both.  BN = 256 keeps its
@@ -100,16 +103,25 @@ struct TcCfg {
     static constexpr int LOAD_BYTES = A_BYTES + B_BYTES;            // what TMA brings per k-block
     static constexpr int STAGE_BYTES = KPS * SUB_BYTES;             // one ring slot
     static constexpr int SMALL_BYTES = KPS * B_BYTES;               // B remainders of one slot
-    // 3xTF32: remainder slots, each with a TMEM stage of A's parts (64 columns
-    // per k-block): 1, 2 or 4 for BN = 256, 128, 64 (2 with two k-blocks per
-    // slot); only BN = 256 also holds B remainders in them.  Within 200 KiB of
-    // ring (224 KiB with two k-blocks per slot).
-    static constexpr int SMALL_STAGES =
-        !SPLIT3 ? 0 : (BN == 256 ? 1 : (BN == 128 ? 2 : (KPS == 2 ? 2 : 4)));
-    static constexpr int SMALL_RING_BYTES = FUSED ? 0 : SMALL_STAGES * SMALL_BYTES;
-    static constexpr int RING_BYTES = (KPS == 2 ? 224 : 200) * 1024;
+    static constexpr int RING_BYTES = (FUSED || KPS == 2 ? 224 : 200) * 1024;
+    // TMEM: the accumulator in columns [0, ACC_COLS) (fused 3xTF32: [0, 2 BN),
+    // the big * small products in the first BN and big * big + small * big in the
+    // second); with SPLIT3 the A operand stages at columns A_TMEM_COL +
+    // A_STAGE_COLS j, 64 per k-block (32 big, then 32 small), all 512 columns
+    // allocated
+    static constexpr int ACC_COLS = FUSED ? 2 * BN : BN;
+    static constexpr uint32_t A_TMEM_COL = FUSED ? ACC_COLS : 256;
+    static constexpr uint32_t A_STAGE_COLS = 64 * KPS;
+    // 3xTF32: remainder slots, each with a TMEM stage of A's parts.  Fused (BN <=
+    // 128): as many TMEM stages as fit beside the accumulator, at most one per
+    // ring slot, so that the transform warps can run that far ahead of the MMAs.
+    // BN = 256: one slot, which also holds B's remainders (a second ring).
+    static constexpr int SMALL_RING_BYTES = FUSED ? 0 : (SPLIT3 ? KPS * B_BYTES : 0);
     static constexpr int STAGES_RAW = (RING_BYTES - SMALL_RING_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int TMEM_STAGES_FIT = static_cast<int>((512 - A_TMEM_COL) / A_STAGE_COLS);
+    static constexpr int SMALL_STAGES =
+        !SPLIT3 ? 0 : (!FUSED ? 1 : (TMEM_STAGES_FIT < STAGES ? TMEM_STAGES_FIT : STAGES));
     // 3xTF32 transform: groups of four warps (one per TMEM lane quarter), group g
     // taking k-blocks g, g + XF_GROUPS, ... so that one group's per-k-block
     // latencies (barrier waits, fences) overlap another group's arithmetic.  A
@@ -123,14 +135,6 @@ struct TcCfg {
     static constexpr int BAR_BYTES = (3 * STAGES + SMALL_STAGES + 1) * 8 + 16;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES +
                                    static_cast<size_t>(SMALL_RING_BYTES) + BAR_BYTES;
-    // TMEM: the accumulator in columns [0, BN) (fused 3xTF32: [0, 2 BN), the
-    // big * small products in the first BN and big * big + small * big in the
-    // second); with SPLIT3 the A operand stages at columns A_TMEM_COL +
-    // A_STAGE_COLS j, 64 per k-block (32 big, then 32 small), all 512 columns
-    // allocated
-    static constexpr int ACC_COLS = FUSED ? 2 * BN : BN;
-    static constexpr uint32_t A_TMEM_COL = 256;
-    static constexpr uint32_t A_STAGE_COLS = 64 * KPS;
     static constexpr uint32_t TMEM_COLS = SPLIT3 ? 512 : BN;  // power of two >= 32
     static_assert(!SPLIT3 || A_TMEM_COL + A_STAGE_COLS * SMALL_STAGES <= 512, "TMEM operand stages");
     static_assert(!SPLIT3 || ACC_COLS <= static_cast<int>(A_TMEM_COL), "accumulator below the operand stages");
