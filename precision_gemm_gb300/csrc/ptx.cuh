@@ -119,6 +119,34 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
     small = x - b;
 }
 
+// split_tf32 over N values at once, for the on-chip splits: the rounding (add
+// half a TF32 unit, clear the 13 low bits) and the exact remainder for every
+// value, then one test for the rare inputs that need split_tf32's care -- an
+// infinite or NaN input, or a finite one whose rounding reaches the all-ones
+// exponent -- which redoes the batch value by value.  Same results as
+// split_tf32 on every input, in fewer instructions per value.
+template <int N>
+__device__ __forceinline__ void split_tf32_batch(const float (&x)[N], uint32_t (&big)[N], uint32_t (&small)[N]) {
+    uint32_t emax = 0;
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        const uint32_t u = __float_as_uint(x[k]);
+        const uint32_t b = (u + 0x1000u) & 0xFFFFE000u;
+        big[k] = b;
+        small[k] = __float_as_uint(x[k] - __uint_as_float(b));
+        emax = max(emax, (u | b) & 0x7F800000u);
+    }
+    if (emax == 0x7F800000u) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            float bf, sf;
+            split_tf32(x[k], bf, sf);
+            big[k] = __float_as_uint(bf);
+            small[k] = __float_as_uint(sf);
+        }
+    }
+}
+
 // Split the BYTES of FP32 values at `tile` (shared memory, TMA-written) in
 // place: each value becomes its TF32 big part and its remainder goes to the same
 // offset in `small`.  A swizzled layout is a function of the byte address inside
@@ -134,15 +162,26 @@ __device__ __forceinline__ void split_tile_in_place(uint8_t* tile, uint8_t* smal
     float4 v[CH];
 #pragma unroll
     for (int c = 0; c < CH; ++c) v[c] = *reinterpret_cast<const float4*>(tile + 16 * (t + c * NTHREADS));
+    constexpr int G = CH < 4 ? CH : 4;  // chunks split per batch
+    static_assert(CH % G == 0, "whole batches");
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-        float4 sm;
-        split_tf32(v[c].x, v[c].x, sm.x);
-        split_tf32(v[c].y, v[c].y, sm.y);
-        split_tf32(v[c].z, v[c].z, sm.z);
-        split_tf32(v[c].w, v[c].w, sm.w);
-        *reinterpret_cast<float4*>(tile + 16 * (t + c * NTHREADS)) = v[c];
-        *reinterpret_cast<float4*>(small + 16 * (t + c * NTHREADS)) = sm;
+    for (int c0 = 0; c0 < CH; c0 += G) {
+        float x[4 * G];
+#pragma unroll
+        for (int c = 0; c < G; ++c) {
+            x[4 * c] = v[c0 + c].x;
+            x[4 * c + 1] = v[c0 + c].y;
+            x[4 * c + 2] = v[c0 + c].z;
+            x[4 * c + 3] = v[c0 + c].w;
+        }
+        uint32_t big[4 * G], sml[4 * G];
+        split_tf32_batch<4 * G>(x, big, sml);
+#pragma unroll
+        for (int c = 0; c < G; ++c) {
+            const int off = 16 * (t + (c0 + c) * NTHREADS);
+            *reinterpret_cast<uint4*>(tile + off) = make_uint4(big[4 * c], big[4 * c + 1], big[4 * c + 2], big[4 * c + 3]);
+            *reinterpret_cast<uint4*>(small + off) = make_uint4(sml[4 * c], sml[4 * c + 1], sml[4 * c + 2], sml[4 * c + 3]);
+        }
     }
 }
 

@@ -387,13 +387,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                             for (int k = 0; k < 16; ++k) a[k] = col[32 * (16 * h + k)];
                         }
                         uint32_t big[16], sml[16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            float b, r;
-                            split_tf32(a[k], b, r);
-                            big[k] = __float_as_uint(b);
-                            sml[k] = __float_as_uint(r);
-                        }
+                        split_tf32_batch<16>(a, big, sml);
                         tmem_st_32x32b_x16(ta + 16 * h, big);
                         tmem_st_32x32b_x16(ta + 32 + 16 * h, sml);
                     }
