@@ -104,13 +104,17 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* statu
 // format: 8-bit exponent, 10 stored mantissa bits), rounded to nearest with
 // ties away from zero by adding half a TF32 unit to the magnitude bits before
 // clearing the low 13 bits.  small = x - big is exact in FP32 (|small| is at
-// most half a TF32 unit of x).  Non-finite inputs pass through as big with a
-// zero remainder; a finite value whose rounding would overflow is truncated.
+// most half a TF32 unit of x); a finite value whose rounding would overflow is
+// truncated.  An infinity becomes big = +-1, small = +-infinity: its products
+// then carry the infinity through the remainder only, so infinity times a
+// finite nonzero value is an infinity of the right sign and times zero is NaN,
+// as in FP32 (with big = infinity, the big * small term would add an infinity
+// of the other remainder's sign, or NaN for a zero remainder).  NaN: both NaN.
 __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
     const uint32_t u = __float_as_uint(x);
     if (!isfinite(x)) {
-        big = x;
-        small = 0.0f;
+        big = isnan(x) ? x : __uint_as_float((u & 0x80000000u) | 0x3F800000u);
+        small = x;
         return;
     }
     float b = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);

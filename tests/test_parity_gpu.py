@@ -285,6 +285,37 @@ def test_forced_split_and_tiles(mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mnk", [(256, 64, 512), (600, 520, 300), (2048, 64, 4096)])
+def test_special_values_match_in_kind(mode, mnk):
+    """Infinities and NaN in A and in B, met by finite values, by zeros and by values
+    whose TF32 remainder is zero, and (FFMA, 3xTF32) the largest float, whose TF32
+    rounding would overflow: every non-finite result must match the oracle's in kind
+    (NaN, or an infinity of the same sign) and every finite one stay within tolerance
+    -- on the single-SM kernel (A split on chip, B on chip or by the pre-pass) and on
+    SM pairs (both split by the pre-pass)."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, alpha=1.0, beta=0.0, dist="normal", seed=73)
+    A, B, C = synth.make(p)
+    a = A[: p.lda * k].view(k, p.lda)    # a[q, i] = A(i, q)
+    b = B[: p.ldb * n].view(n, p.ldb)    # b[j, q] = B(q, j)
+    inf, nan = float("inf"), float("nan")
+    a[3, 1], a[7, 5], a[11, 9] = inf, -inf, nan
+    b[:, 3] = torch.round(b[:, 3] * 2)          # integers (zero remainder), some of them 0
+    b[:, 7] = torch.round(b[:, 7] * 2)
+    b[2, 20], b[4, 21], b[6, 20] = inf, nan, -inf
+    if mode != "tf32":
+        a[17, 13] = float(np.finfo(np.float32).max)
+        b[:, 17] = b[:, 17].clamp(-1.0, 1.0) * 0.5   # keeps FLT_MAX * b inside FP32
+    out, ok = H.run_gpu(p, mode, A, B, C)
+    assert ok
+    cref, den = H.reference_full(p, A, B, C)
+    got = H.logical(p, out)
+    assert (~np.isfinite(cref)).sum() > 0
+    res = oracle.check(got, cref, den, oracle.TOL[mode])
+    assert res["ok"], res
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_beta_zero_ignores_nan_c(mode):
     p = synth.Problem(200, 150, 100, alpha=1.0, beta=0.0, dist="normal", seed=17)
     A, B, C = synth.make(p)
