@@ -289,7 +289,7 @@ def run_ours(args, wl_name):
         "metric": "SGEMM TFLOPS (2MNK/s) at 4096^3/8192^3 fp32; % of FP32 & TF32 peak",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see DESIGN.md input recipe)",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded CPU draws: A, B and C_in in storage order, padding set to NaN)",
         "config": {"workload": desc, "name": wl_name, "m": p.m, "n": p.n, "k": p.k, "modes": modes,
                    "layout": p.layout, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (no flush)" if alg_bytes > 129e6 else "L2 not flushed; inputs fit"},
