@@ -32,6 +32,12 @@
  *     thread.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream) unless stated otherwise.
+ *   - Threads: calls on different streams may come from any host threads at
+ *     once.  Calls on ONE stream must not overlap in time on the host (make
+ *     them from one thread, or hold a lock around each call): a call that needs
+ *     a larger workspace than the stream's frees the old one in stream order,
+ *     so a concurrent call that took the old workspace's address could enqueue
+ *     its kernels after that free.
  *   - A failure detected inside a running kernel (a bounded wait that
  *     expired) cannot be returned by the launching call; it is recorded in a
  *     per-device status word that sgemm_device_status() reads.
