@@ -370,7 +370,8 @@ def run_reference(args, wl_name):
               if p.layout == "col" else ("N", "N", p.n, p.m, p.k, p.alpha, B, p.ldb, A, p.lda, p.beta, C, p.ldc))
     mm, nn = args_o[2], args_o[3]
     rng = np.random.default_rng(7)
-    budget = max(2.0, min(15.0, 150.0 / max(1, args.steps + args.warmup)))
+    budget = (args.ref_step_seconds if args.ref_step_seconds else
+              max(2.0, min(15.0, 150.0 / max(1, args.steps + args.warmup))))
     probe = max(nthreads, 64)
     t0 = time.perf_counter()
     O.entries(*args_o, rng.integers(0, mm, probe), rng.integers(0, nn, probe), threads=nthreads)
@@ -409,6 +410,8 @@ def main():
     ap.add_argument("--cpu-threads", type=int, default=0)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-seconds", type=float, default=0.0,
+                    help="reference arm: CPU seconds per step (default: the run bounded to ~150 s)")
     ap.add_argument("--fma-ceiling", action="store_true",
                     help="run only the register-only FP32 FMA throughput probe and print its JSON line")
     ap.add_argument("--tf32-ceiling", action="store_true",

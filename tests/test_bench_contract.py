@@ -1,0 +1,61 @@
+"""The benchmark's output contract, on the arm that needs no GPU (CPU only).
+
+`bench.py --impl reference` times the oracle on host cores and prints one JSON
+line with the same metric, unit and config as the GPU arm, plus the oracle's
+own cpu_baseline and an e2e object with no host-device traffic.  Under a
+multi-process launch only rank 0 prints; the other ranks exit 0 without work.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*argv, env_extra=None, timeout=240):
+    env = {**os.environ, **(env_extra or {})}
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *argv], capture_output=True, text=True,
+                          timeout=timeout, env=env, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    proc = _bench("--impl", "reference", "--workload", "ragged", "--steps", "2", "--warmup", "1",
+                  "--cpu-threads", "2", "--ref-step-seconds", "0.3")
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    lines = [ln for ln in proc.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, proc.stdout
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["metric"].startswith("SGEMM TFLOPS") and line["unit"] == "TFLOP/s"
+    assert line["value"] > 0 and line["ms_per_step"] > 0 and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 3  # warm-up raised to the three-step minimum
+    assert line["n_gpus"] == 1 and line["vs_baseline"] is None
+    cfg = line["config"]
+    assert (cfg["m"], cfg["n"], cfg["k"]) == (3000, 1500, 777) and "3000x1500x777" in cfg["workload"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["unit"] == line["unit"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    proc = _bench("--impl", "reference", "--workload", "ragged", "--steps", "1", "--warmup", "3",
+                  "--ref-step-seconds", "0.3", env_extra={"RANK": "1", "WORLD_SIZE": "2"}, timeout=120)
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    assert proc.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("flag", ["--help"])
+def test_cli_lists_the_contract_flags(flag):
+    proc = _bench(flag, timeout=120)
+    assert proc.returncode == 0
+    for opt in ("--gpus", "--steps", "--warmup", "--impl"):
+        assert opt in proc.stdout
