@@ -106,8 +106,12 @@ extern "C" {
  * for operand copies, 3xTF32 split operands and split-K partial sums; it grows
  * on demand with stream-ordered allocation and is released by
  * sgemm_workspace_release().  Calls on the same stream are ordered; calls on
- * different streams use different workspaces.  A null pointer is an invalid
- * argument only when the call would read or write through it.
+ * different streams use different workspaces.  The workspaces are keyed by
+ * the stream handle and outlive the stream: synchronise a stream before
+ * destroying it (a stream created later may get the same handle, and with it
+ * the cached workspace), and call sgemm_workspace_release() to free them.  A
+ * null pointer is an invalid argument only when the call would read or write
+ * through it.
  *
  * Results are deterministic: the same inputs, mode and device give bitwise
  * identical C on every run (split-K partial sums are added in a fixed order).
