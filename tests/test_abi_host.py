@@ -288,3 +288,45 @@ def test_plan_struct_layout_matches_header(lib, tmp_path):
     for f in fields:
         assert int(out[f]) == getattr(pg.sgemm_plan_t, f).offset, f
     assert int(out["size"]) == ctypes.sizeof(pg.sgemm_plan_t)
+
+
+def test_plain_c_caller_links_and_calls_the_library(lib, tmp_path):
+    """A C program with no Python or torch in it links the shared library and
+    calls it through the header alone: the version, the planner on a device it
+    does not touch, an invalid argument answered with -i and a message, and a
+    call with nothing to do."""
+    src = tmp_path / "caller.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "precision_gemm.h"
+int main(void) {
+    sgemm_plan_t p;
+    if (!strstr(sgemm_version(), "sm_103a")) return 1;
+    if (sgemm_plan('N', 'N', 8192, 8192, 8192, 1.0f, (const void *)4096, 8192, (const void *)8192, 8192, 1.0f,
+                   (const void *)16384, 8192, SGEMM_TF32, 152, &p) != 0) return 2;
+    if (p.kernel != SGEMM_KERNEL_TC2 || p.bm != 256 || p.bn != 512 || p.split_k != 1) return 3;
+    if (sgemm_plan('T', 'N', 3000, 1500, 777, 1.5f, (const void *)4100, 777, (const void *)8192, 784, -0.5f,
+                   (const void *)16384, 3005, SGEMM_FFMA, 152, &p) != 0) return 4;
+    if (p.kernel != SGEMM_KERNEL_FFMA || p.prep_a != SGEMM_PREP_TRANSPOSE || p.prep_b != SGEMM_PREP_NONE) return 5;
+    if (sgemm('N', 'N', 64, 48, 32, 1.0f, (const float *)4096, 63, (const float *)8192, 32, 0.0f,
+              (float *)16384, 64, SGEMM_FFMA, NULL) != -8) return 6;
+    if (!strstr(sgemm_last_error_string(), "argument 8")) return 7;
+    if (sgemm_plan('N', 'N', 64, 48, 32, 1.0f, NULL, 64, NULL, 32, 0.0f, NULL, 64, 7, 152, &p) != -7) return 8;
+    if (sgemm_plan('N', 'N', 64, 48, 32, 1.0f, (const void *)4096, 64, (const void *)8192, 32, 0.0f,
+                   (const void *)16384, 64, 7, 152, &p) != -14) return 10;
+    if (sgemm('N', 'N', 0, 48, 32, 1.0f, NULL, 1, NULL, 32, 0.0f, NULL, 1, SGEMM_3XTF32, NULL) != 0) return 9;
+    puts("ok");
+    return 0;
+}
+''')
+    libdir = os.path.dirname(pg.LIB_PATH)
+    libname = os.path.basename(pg.LIB_PATH)
+    assert libname.startswith("lib") and libname.endswith(".so")
+    exe = tmp_path / "caller"
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-L", libdir, "-l" + libname[3:-3], "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stdout, run.stderr)
