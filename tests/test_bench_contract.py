@@ -59,3 +59,23 @@ def test_cli_lists_the_contract_flags(flag):
     assert proc.returncode == 0
     for opt in ("--gpus", "--steps", "--warmup", "--impl"):
         assert opt in proc.stdout
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """The launch the scaling run uses (torchrun, two ranks on this host): rank 0
+    alone prints the line, every rank exits 0."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    proc = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                           "--gpus", "2", "--impl", "reference", "--workload", "ragged", "--steps", "1",
+                           "--warmup", "3", "--cpu-threads", "2", "--ref-step-seconds", "0.3"],
+                          capture_output=True, text=True, timeout=300, cwd=ROOT,
+                          env={**os.environ, "OMP_NUM_THREADS": "2"})
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    lines = [ln for ln in proc.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, proc.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
