@@ -386,3 +386,40 @@ def test_planted_mistake_is_caught(tmp_path, name):
 
 def test_unmutated_oracle_passes_every_pin(oracle_lib):
     assert _run_pins(oracle_lib) == []
+
+
+def test_acceptance_workloads_match_their_specification():
+    """The named workloads carry the acceptance suite's sizes, leading dimensions,
+    scalars, distributions and seed, and their draws have the stated ranges."""
+    P = synth.config_problems()
+    want = {
+        "c1_256": (256, 256, 256, 256, 256, 256, 1.0, 0.0, "uniform", "uniform", "col"),
+        "c2_rm1024": (1024, 1024, 1024, 1024, 1024, 1024, 1.0, 0.0, "uniform", "uniform", "row"),
+        "c2_rm2048": (2048, 2048, 2048, 2048, 2048, 2048, 1.0, 0.0, "uniform", "uniform", "row"),
+        "c2_rm4096": (4096, 4096, 4096, 4096, 4096, 4096, 1.0, 0.0, "uniform", "uniform", "row"),
+        # ragged: lda = m + 13, ldb = k + 7, ldc = m + 5, C_in ~ N(0, 1)
+        "c3_ragged": (3000, 1500, 777, 3013, 784, 3005, 1.5, -0.5, "normal", "normal", "col"),
+        "c4_8192": (8192, 8192, 8192, 8192, 8192, 8192, 1.0, 1.0, "uniform", "uniform", "col"),
+        "c4_16384": (16384, 16384, 16384, 16384, 16384, 16384, 1.0, 1.0, "uniform", "uniform", "col"),
+        "c5a_16384x16384x64": (16384, 16384, 64, 16384, 64, 16384, 1.0, 0.0, "normal", "normal", "col"),
+        "c5b_128x128x262144": (128, 128, 262144, 128, 262144, 128, 1.0, 0.0, "normal", "normal", "col"),
+        "c5c_8192x64x8192": (8192, 64, 8192, 8192, 8192, 8192, 1.0, 0.0, "normal", "normal", "col"),
+    }
+    assert sorted(P) == sorted(want)
+    for name, (m, n, k, lda, ldb, ldc, alpha, beta, dist, c_dist, layout) in want.items():
+        p = P[name]
+        got = (p.m, p.n, p.k, p.lda, p.ldb, p.ldc, p.alpha, p.beta, p.dist, p.c_dist, p.layout)
+        assert got == (m, n, k, lda, ldb, ldc, alpha, beta, dist, c_dist, layout), name
+        assert p.transa == "N" and p.transb == "N" and p.seed == 0, name
+    # draws: U[-1, 1) and N(0, 1); the ragged problem's padding rows hold the NaN sentinel
+    A, B, C = synth.make(P["c1_256"])
+    for x in (A, B):
+        assert float(x.min()) >= -1.0 and float(x.max()) < 1.0 and abs(float(x.mean())) < 0.01
+    A, B, C = synth.make(P["c3_ragged"])
+    a = A.view(777, 3013)
+    assert torch.all(a[:, 3000:].view(torch.int32) == synth.NAN_BITS)
+    body = a[:, :3000]
+    assert torch.isfinite(body).all() and abs(float(body.mean())) < 0.01 and abs(float(body.std()) - 1) < 0.01
+    assert torch.all(B.view(1500, 784)[:, 777:].view(torch.int32) == synth.NAN_BITS)
+    assert torch.all(C.view(1500, 3005)[:, 3000:].view(torch.int32) == synth.NAN_BITS)
+    assert abs(float(C.view(1500, 3005)[:, :3000].std()) - 1) < 0.01
