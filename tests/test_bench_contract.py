@@ -79,3 +79,44 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, proc.stdout
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def _profile_commands(text):
+    """Logical command lines (backslash continuations joined) of a profile summary."""
+    out, cur = [], ""
+    for raw in text.splitlines():
+        line = raw.strip()
+        if not cur and not (line.startswith("ncu ") or line.startswith("python ") or line.startswith("SNIP=")):
+            continue
+        cur += " " + line.rstrip("\\").strip()
+        if not line.endswith("\\"):
+            out.append(cur.strip())
+            cur = ""
+    return out
+
+
+def test_profile_summaries_give_runnable_commands():
+    """Each ncu summary under profiles/ names the command that made it; the
+    command runs committed files only, with bench.py flags and workloads that
+    exist, and every ncu invocation leaves the clocks alone."""
+    import re
+    sys.path.insert(0, ROOT)
+    import bench
+    help_text = _bench("--help", timeout=120).stdout
+    pdir = os.path.join(ROOT, "profiles")
+    names = sorted(f for f in os.listdir(pdir) if f.endswith(".md"))
+    assert names
+    for name in names:
+        cmds = _profile_commands(open(os.path.join(pdir, name)).read())
+        assert any(c.startswith("ncu ") for c in cmds), name
+        for c in cmds:
+            if c.startswith("ncu "):
+                assert "--clock-control none" in c, (name, c)
+            if "bench.py" in c:
+                tail = c.split("bench.py", 1)[1].split()
+                for tok in tail:
+                    if tok.startswith("--"):
+                        assert tok in help_text, (name, tok)
+                m = re.search(r"--workload (\S+)", c)
+                if m:
+                    assert m.group(1) in bench.WORKLOADS, (name, m.group(1))
