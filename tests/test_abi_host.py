@@ -316,6 +316,10 @@ int main(void) {
     if (sgemm_plan('N', 'N', 64, 48, 32, 1.0f, (const void *)4096, 64, (const void *)8192, 32, 0.0f,
                    (const void *)16384, 64, 7, 152, &p) != -14) return 10;
     if (sgemm('N', 'N', 0, 48, 32, 1.0f, NULL, 1, NULL, 32, 0.0f, NULL, 1, SGEMM_3XTF32, NULL) != 0) return 9;
+    if (sgemm_plan('N', 'N', 64, 48, 32, 1.0f, (const void *)4096, 64, (const void *)8192, 32, 0.0f,
+                   (const void *)16384, 64, SGEMM_FFMA, 0, &p) != -15) return 11;
+    if (sgemm_plan('N', 'N', 64, 48, 32, 1.0f, (const void *)4096, 64, (const void *)8192, 32, 0.0f,
+                   (const void *)16384, 64, SGEMM_FFMA, 152, NULL) != -16) return 12;
     puts("ok");
     return 0;
 }
