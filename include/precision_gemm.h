@@ -71,6 +71,8 @@ extern "C" {
                                   captured into a CUDA graph                    */
 #define SGEMM_ERR_SCRATCH 8    /* sgemm_noalloc: the call needs more scratch than
                                   its fixed device array holds                  */
+#define SGEMM_ERR_WORKSPACE 9  /* the workspace given by sgemm_set_workspace is
+                                  smaller than the call needs                   */
 
 /* Kernel families reported by sgemm_plan(). */
 #define SGEMM_KERNEL_NONE 0    /* nothing to do (m == 0, n == 0, or C unchanged) */
@@ -105,7 +107,8 @@ extern "C" {
  * on `stream` completes.  The library owns a workspace per (device, stream)
  * for operand copies, 3xTF32 split operands and split-K partial sums; it grows
  * on demand with stream-ordered allocation and is released by
- * sgemm_workspace_release().  Calls on the same stream are ordered; calls on
+ * sgemm_workspace_release() -- unless the caller has given the stream a
+ * workspace of its own with sgemm_set_workspace().  Calls on the same stream are ordered; calls on
  * different streams use different workspaces.  The workspaces are keyed by
  * the stream handle and outlive the stream: synchronise a stream before
  * destroying it (a stream created later may get the same handle, and with it
@@ -164,13 +167,18 @@ int sgemm_host_async(char transa, char transb, int64_t m, int64_t n, int64_t k, 
  * partial sums, lives in a fixed 16 MiB array in device memory that every
  * GPU loading the library holds until the process exits.
  *
- * Arguments are those of sgemm, with these limits: mode is SGEMM_FFMA or
- * SGEMM_TF32 (else -14); transa and transb are 'N' (else -1, -2); A and B are
- * 16-byte aligned with lda and ldb multiples of 4 (else -7/-8, -9/-10), so the
- * kernels read them in place; and the call's split-K partial sums,
- * split_k * round_up(m, 4) * n * 4 bytes as sgemm_plan reports split_k, fit in
- * the 16 MiB array (else SGEMM_ERR_SCRATCH, and nothing is launched).  Results
- * equal sgemm's for the same arguments.
+ * Arguments are those of sgemm.  When the call reads A and B (k > 0 and
+ * alpha != 0) these limits apply, checked in signature order: transa and
+ * transb are 'N' (else -1, -2); A and B are 16-byte aligned with lda and ldb
+ * multiples of 4 (else -7/-8, -9/-10), so the kernels read them in place; mode
+ * is SGEMM_FFMA or SGEMM_TF32 (else -14).  A call that only scales C
+ * (k == 0 or alpha == 0) takes any arguments sgemm takes.  The call's split-K
+ * partial sums, split_k * round_up(m, 4) * n * 4 bytes as sgemm_plan reports
+ * split_k, must fit in the 16 MiB array (else SGEMM_ERR_SCRATCH, and nothing
+ * is launched).  sgemm_noalloc never splits the last partial wave of tiles
+ * along K as sgemm may (sgemm_plan's tail_split > 1), so its results equal
+ * sgemm's within the mode's tolerance, and bit for bit when sgemm_plan
+ * reports tail_split == 1.
  *
  * The first call on a device takes the array's device address (a
  * cudaGetSymbolAddress call with that device current, done once per device);
@@ -183,6 +191,40 @@ int sgemm_host_async(char transa, char transb, int64_t m, int64_t n, int64_t k, 
 int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha,
                   const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                   float *C, int64_t ldc, int mode, void *stream);
+
+/*
+ * sgemm_set_workspace -- give the library device memory to use as the
+ * workspace of calls on `stream` (a cudaStream_t as void*, NULL for the legacy
+ * default stream) on the current device, instead of memory it allocates
+ * itself: for callers whose device memory comes from their own allocator (a
+ * framework's caching allocator, a memory pool reserved at start-up).  The
+ * pages have no counterpart; the lecture's host routine allocates its device
+ * arrays itself.
+ *
+ *   workspace  device memory of the current device, 256-byte aligned (1), or
+ *              NULL to return the stream to the library's own workspace
+ *   bytes      its size; 0 when workspace is NULL (2).  The buffer must lie
+ *              inside one allocation (checked when the driver can tell)
+ *   stream     the stream whose calls use it (3)
+ *
+ * sgemm, and the product step of sgemm_host / sgemm_host_async, on that
+ * stream then take their workspace (operand copies, 3xTF32 split operands,
+ * split-K and last-wave partial sums: sgemm_plan's workspace_bytes) from this
+ * buffer and never allocate one; a call needing more than `bytes` returns
+ * SGEMM_ERR_WORKSPACE before launching anything.  The host entries' staging
+ * buffers (the device copies of host A, B and C) are still the library's.
+ * Setting a buffer frees the library's own workspace for that stream in stream
+ * order (SGEMM_ERR_CAPTURE if the stream is being captured).
+ *
+ * Ownership: the caller owns the buffer and keeps it alive, unwritten by
+ * anything else, until the work queued on `stream` by the calls that used it
+ * has completed, and until another sgemm_set_workspace call replaces it for
+ * that stream.  Calls on one stream are ordered and may share the buffer;
+ * giving one buffer to two streams makes their calls race.
+ * sgemm_workspace_release does not touch it.  Returns 0, -i for an invalid
+ * argument, or SGEMM_ERR_NO_DEVICE / SGEMM_ERR_ARCH.
+ */
+int sgemm_set_workspace(void *workspace, size_t bytes, void *stream);
 
 /* The choices sgemm would make for a call (see sgemm_plan). */
 typedef struct sgemm_plan {
@@ -253,7 +295,8 @@ int sgemm_debug_flags(int flags);
 /* Kernels this library has launched in this process (all devices). */
 uint64_t sgemm_launch_count(void);
 
-/* Free every cached workspace and staging buffer (synchronises the device). */
+/* Free every cached workspace and staging buffer the library allocated
+ * (synchronises the device); buffers given by sgemm_set_workspace stay in use. */
 int sgemm_workspace_release(void);
 
 /* Human-readable description of the last failure on the calling thread. */

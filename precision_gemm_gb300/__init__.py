@@ -12,6 +12,12 @@ A, B, C are device pointers (ints) or CUDA torch tensors (their storage is
 addressed through ``data_ptr()``); mode is 'ffma', 'tf32', '3xtf32' or the
 integer SGEMM_* constant; stream is a torch.cuda.Stream, a raw handle, or None
 for torch's current stream.
+
+Tensor operands are checked before the library is called, for every operand
+the call reads or writes: float32, on the current CUDA device (host memory for
+the sgemm_host entries), and a storage that holds the operand's whole extent
+(ld * (cols - 1) + rows elements from the tensor's first element).  A failed
+check raises ValueError.  Integer addresses are passed on unchecked.
 """
 from __future__ import annotations
 
@@ -27,15 +33,19 @@ MODES = {"ffma": SGEMM_FFMA, "tf32": SGEMM_TF32, "3xtf32": SGEMM_3XTF32}
 MODE_NAMES = {v: k for k, v in MODES.items()}
 
 SGEMM_ERR = {1: "SGEMM_ERR_CUDA", 2: "SGEMM_ERR_NO_DEVICE", 3: "SGEMM_ERR_ARCH", 4: "SGEMM_ERR_TIMEOUT",
-             5: "SGEMM_ERR_ALLOC", 6: "SGEMM_ERR_TENSOR_MAP", 7: "SGEMM_ERR_CAPTURE", 8: "SGEMM_ERR_SCRATCH"}
+             5: "SGEMM_ERR_ALLOC", 6: "SGEMM_ERR_TENSOR_MAP", 7: "SGEMM_ERR_CAPTURE", 8: "SGEMM_ERR_SCRATCH",
+             9: "SGEMM_ERR_WORKSPACE"}
+SGEMM_ERR_CAPTURE = 7
 SGEMM_ERR_SCRATCH = 8
+SGEMM_ERR_WORKSPACE = 9
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_DEBUG_STALL_PRODUCER = 1
 KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc", 4: "tc2"}
 PREPS = {0: "none", 1: "copy", 2: "transpose", 3: "split"}
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTS = ("sgemm", "sgemm_host", "sgemm_host_async", "sgemm_noalloc", "sgemm_plan", "sgemm_device_status",
+EXPORTS = ("sgemm", "sgemm_host", "sgemm_host_async", "sgemm_noalloc", "sgemm_set_workspace", "sgemm_plan",
+           "sgemm_device_status",
            "sgemm_set_wait_timeout", "sgemm_force_plan", "sgemm_debug_flags", "sgemm_launch_count",
            "sgemm_workspace_release", "sgemm_last_error_string", "sgemm_version")
 
@@ -83,6 +93,8 @@ def load_library(path: str | None = None):
         lib.sgemm_host_async.restype = i
         lib.sgemm_noalloc.argtypes = gemm_args
         lib.sgemm_noalloc.restype = i
+        lib.sgemm_set_workspace.argtypes = [vp, ctypes.c_size_t, vp]
+        lib.sgemm_set_workspace.restype = i
         lib.sgemm_plan.argtypes = gemm_args[:14] + [i, ctypes.POINTER(sgemm_plan_t)]
         lib.sgemm_plan.restype = i
         lib.sgemm_device_status.argtypes = [vp, i]
@@ -118,6 +130,70 @@ def _ptr(x) -> int:
     raise TypeError("cannot take a pointer from %r" % type(x))
 
 
+def _notrans(t) -> bool:
+    return _tchar(t) in (b"N", b"n")
+
+
+def _extent(rows: int, cols: int, ld: int) -> int:
+    """Elements from the first one that a rows x cols column-major operand with
+    leading dimension ld spans (the last column needs only its rows)."""
+    return 0 if rows <= 0 or cols <= 0 else ld * (cols - 1) + rows
+
+
+def _check_operand(x, name: str, rows: int, cols: int, ld: int, on_device: bool) -> None:
+    """Raise ValueError unless tensor / array x can serve as a rows x cols operand
+    with leading dimension ld: float32, in device memory of the current CUDA
+    device (on_device) or in host memory (not on_device), with storage for the
+    whole extent.  ints are not checked; None is left to the library, which
+    rejects a null pointer the call needs."""
+    if x is None or isinstance(x, int):
+        return
+    if hasattr(x, "untyped_storage"):  # torch tensor
+        import torch
+        if x.dtype != torch.float32:
+            raise ValueError("%s: expected a float32 tensor, got %s" % (name, x.dtype))
+        if on_device:
+            if not x.is_cuda:
+                raise ValueError("%s: expected a CUDA tensor, got one on %s" % (name, x.device))
+            cur = torch.cuda.current_device()
+            if x.device.index != cur:
+                raise ValueError("%s: the tensor is on %s, the current device is cuda:%d" % (name, x.device, cur))
+        elif x.is_cuda:
+            raise ValueError("%s: expected a host (CPU) tensor, got one on %s" % (name, x.device))
+        avail = (x.untyped_storage().nbytes() - x.storage_offset() * x.element_size()) // 4
+    elif hasattr(x, "ctypes") and hasattr(x, "dtype"):  # numpy array
+        if on_device:
+            raise ValueError("%s: a numpy array is host memory; this call takes device memory" % name)
+        if str(x.dtype) != "float32":
+            raise ValueError("%s: expected a float32 array, got %s" % (name, x.dtype))
+        if not (x.flags["C_CONTIGUOUS"] or x.flags["F_CONTIGUOUS"]):
+            raise ValueError("%s: the array must be contiguous" % name)
+        avail = int(x.size)
+    else:
+        raise TypeError("%s: cannot take a pointer from %r" % (name, type(x)))
+    if ld < max(1, rows):
+        return  # the library reports the bad leading dimension as an invalid argument
+    need = _extent(rows, cols, ld)
+    if avail < need:
+        raise ValueError("%s: a %d x %d operand with leading dimension %d spans %d elements; the storage from the "
+                         "tensor's first element holds %d" % (name, rows, cols, ld, need, avail))
+
+
+def _check_gemm_operands(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, on_device: bool) -> None:
+    """The operand checks of one call: A and B when the product reads them, C when
+    the call reads or writes it (the library's own rules for what it touches)."""
+    if m <= 0 or n <= 0:
+        return
+    reads_ab = k > 0 and alpha != 0.0
+    if reads_ab:
+        ra, ca = (m, k) if _notrans(transa) else (k, m)
+        rb, cb = (k, n) if _notrans(transb) else (n, k)
+        _check_operand(A, "A", ra, ca, lda, on_device)
+        _check_operand(B, "B", rb, cb, ldb, on_device)
+    if reads_ab or beta != 1.0:
+        _check_operand(C, "C", m, n, ldc, on_device)
+
+
 def _stream(s) -> int:
     if s is None:
         import torch
@@ -145,6 +221,7 @@ def _tchar(t: str) -> bytes:
 def sgemm(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma", stream=None) -> None:
     """C = alpha*op(A)*op(B) + beta*C on device memory (column-major); asynchronous."""
     lib = load_library()
+    _check_gemm_operands(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, on_device=True)
     _check(lib.sgemm(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                      _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
 
@@ -152,6 +229,7 @@ def sgemm(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ff
 def sgemm_host(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma", stream=None) -> None:
     """The same on host arrays (pinned tensors / numpy); returns when C holds the result."""
     lib = load_library()
+    _check_gemm_operands(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, on_device=False)
     _check(lib.sgemm_host(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                           _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
 
@@ -161,6 +239,7 @@ def sgemm_host_async(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ld
     """sgemm_host queued on `stream` without waiting: C holds the result once the
     stream is synchronised; until then A, B and C must stay untouched (and alive)."""
     lib = load_library()
+    _check_gemm_operands(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, on_device=False)
     _check(lib.sgemm_host_async(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                                 _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
 
@@ -173,6 +252,7 @@ def sgemm_noalloc(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, 
     aligned operands with ld multiples of 4; raises SgemmError (code
     SGEMM_ERR_SCRATCH) when the call's partial sums would not fit."""
     lib = load_library()
+    _check_gemm_operands(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, on_device=True)
     _check(lib.sgemm_noalloc(_tchar(transa), _tchar(transb), m, n, k, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                              _ptr(C), ldc, _mode(mode), _stream(stream)), lib)
 
@@ -183,6 +263,46 @@ def sgemm_rm(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma", stream=N
     column-major storage of the transpose, so this is the column-major call
     C^T = B^T * A^T: operands swapped, m and n swapped."""
     sgemm("N", "N", n, m, k, alpha, B, ldb, A, lda, beta, C, ldc, mode, stream)
+
+
+_ws_refs = {}  # (device, stream handle) -> the tensor given to set_workspace, kept alive here
+
+
+def set_workspace(buf, nbytes: int | None = None, stream=None) -> None:
+    """Give calls on `stream` (torch's current stream when None) on the current
+    device a workspace of the caller's own instead of one the library allocates:
+    a CUDA tensor (its storage from its first element; 256-byte aligned, as the
+    caching allocator gives) or an integer address with nbytes; None returns the
+    stream to the library's own workspace.  The tensor is kept alive here until
+    it is replaced.  Calls needing more than its size raise SgemmError with code
+    SGEMM_ERR_WORKSPACE; sgemm_plan(...)["workspace_bytes"] gives the need."""
+    lib = load_library()
+    st = _stream(stream)
+    if buf is None:
+        ptr, size = 0, 0
+    elif isinstance(buf, int):
+        if nbytes is None:
+            raise ValueError("an integer workspace address needs nbytes")
+        ptr, size = buf, int(nbytes)
+    else:
+        import torch
+        if not getattr(buf, "is_cuda", False):
+            raise ValueError("the workspace must be a CUDA tensor")
+        if buf.device.index != torch.cuda.current_device():
+            raise ValueError("the workspace is on %s, the current device is cuda:%d"
+                             % (buf.device, torch.cuda.current_device()))
+        avail = buf.untyped_storage().nbytes() - buf.storage_offset() * buf.element_size()
+        size = avail if nbytes is None else int(nbytes)
+        if size > avail:
+            raise ValueError("nbytes %d exceeds the tensor's storage (%d bytes)" % (size, avail))
+        ptr = int(buf.data_ptr())
+    _check(lib.sgemm_set_workspace(ptr, size, st), lib)
+    import torch
+    key = (torch.cuda.current_device() if torch.cuda.is_available() else 0, st)
+    if buf is None:
+        _ws_refs.pop(key, None)
+    else:
+        _ws_refs[key] = buf
 
 
 def sgemm_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma",

@@ -328,11 +328,29 @@ struct Buf {
 };
 std::mutex g_ws_mu;
 std::map<std::pair<std::pair<int, uintptr_t>, int>, Buf> g_bufs;
+// Workspaces supplied by the caller (sgemm_set_workspace), per (device, stream):
+// used in place of the library's own workspace buffer, never grown or freed here.
+std::map<std::pair<int, uintptr_t>, Buf> g_user_ws;
+
+constexpr int kPurposeWorkspace = 0;
+constexpr int kPurposeStaging = 1;
 
 int get_buffer(int dev, cudaStream_t st, int purpose, size_t need, void** out) {
     *out = nullptr;
     if (need == 0) return 0;
     std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (purpose == kPurposeWorkspace) {
+        auto u = g_user_ws.find({dev, reinterpret_cast<uintptr_t>(st)});
+        if (u != g_user_ws.end()) {
+            if (u->second.bytes < need)
+                return fail(SGEMM_ERR_WORKSPACE,
+                            "the call needs %zu bytes of workspace; the workspace given by sgemm_set_workspace for "
+                            "this stream holds %zu",
+                            need, u->second.bytes);
+            *out = u->second.ptr;
+            return 0;
+        }
+    }
     Buf& b = g_bufs[{{dev, reinterpret_cast<uintptr_t>(st)}, purpose}];
     if (b.bytes >= need) {
         *out = b.ptr;
@@ -361,8 +379,29 @@ int get_buffer(int dev, cudaStream_t st, int purpose, size_t need, void** out) {
     return 0;
 }
 
-constexpr int kPurposeWorkspace = 0;
-constexpr int kPurposeStaging = 1;
+// [base, base + size) of the device allocation holding `p` (driver call
+// cuMemGetAddressRange, reached through the runtime's entry-point query), or
+// false when the driver cannot say.
+bool allocation_range(const void* p, uintptr_t* base, size_t* size) {
+    using RangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+    static std::once_flag once;
+    static RangeFn fn = nullptr;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &q, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<RangeFn>(q);
+    });
+    if (!fn) return false;
+    CUdeviceptr b = 0;
+    size_t s = 0;
+    if (fn(&b, &s, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return false;
+    *base = static_cast<uintptr_t>(b);
+    *size = s;
+    return true;
+}
 
 // ---- TMA tensor maps ------------------------------------------------------------------
 
@@ -668,15 +707,21 @@ int noalloc_scratch(int dev, float** out) {
 int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
                 int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
                 cudaStream_t st) {
-    if (mode != SGEMM_FFMA && mode != SGEMM_TF32)
-        return fail(-14, "argument 14 (mode): sgemm_noalloc supports SGEMM_FFMA and SGEMM_TF32 only (3xTF32 needs "
-                         "split operands in a workspace)");
-    if (!is_notrans(transa)) return fail(-1, "argument 1 (transa): sgemm_noalloc reads A untransposed ('N')");
-    if (!is_notrans(transb)) return fail(-2, "argument 2 (transb): sgemm_noalloc reads B untransposed ('N')");
-    if (!aligned16(A)) return fail(-7, "argument 7 (A): sgemm_noalloc needs a 16-byte aligned A");
-    if (lda % 4 != 0) return fail(-8, "argument 8 (lda): sgemm_noalloc needs lda to be a multiple of 4");
-    if (!aligned16(B)) return fail(-9, "argument 9 (B): sgemm_noalloc needs a 16-byte aligned B");
-    if (ldb % 4 != 0) return fail(-10, "argument 10 (ldb): sgemm_noalloc needs ldb to be a multiple of 4");
+    // The limits below concern how the kernels read A and B in place; a call that
+    // only scales C (k == 0 or alpha == 0) reads neither and is not limited.
+    // Checked in signature order.
+    const bool reads_ab = k > 0 && alpha != 0.0f;
+    if (reads_ab) {
+        if (!is_notrans(transa)) return fail(-1, "argument 1 (transa): sgemm_noalloc reads A untransposed ('N')");
+        if (!is_notrans(transb)) return fail(-2, "argument 2 (transb): sgemm_noalloc reads B untransposed ('N')");
+        if (!aligned16(A)) return fail(-7, "argument 7 (A): sgemm_noalloc needs a 16-byte aligned A");
+        if (lda % 4 != 0) return fail(-8, "argument 8 (lda): sgemm_noalloc needs lda to be a multiple of 4");
+        if (!aligned16(B)) return fail(-9, "argument 9 (B): sgemm_noalloc needs a 16-byte aligned B");
+        if (ldb % 4 != 0) return fail(-10, "argument 10 (ldb): sgemm_noalloc needs ldb to be a multiple of 4");
+        if (mode != SGEMM_FFMA && mode != SGEMM_TF32)
+            return fail(-14, "argument 14 (mode): sgemm_noalloc supports SGEMM_FFMA and SGEMM_TF32 only (3xTF32 "
+                             "needs split operands in a workspace)");
+    }
     int dev;
     DeviceState* ds;
     int rc = current_device(&dev, &ds);
@@ -691,12 +736,15 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
         return 0;
     }
     const int64_t ldp = round_up(m, 4);
-    const size_t need = pl.split_k > 1 ? static_cast<size_t>(pl.split_k) * ldp * n * sizeof(float) : 0;
-    if (need > kNoAllocScratchBytes)
+    // split_k * ldp * n floats must fit; compared by division so that no product
+    // can wrap (ldp * n < 2^62 by the size limits, split_k <= 65535).
+    if (pl.split_k > 1 &&
+        ldp * n > static_cast<int64_t>(kNoAllocScratchBytes / sizeof(float)) / pl.split_k)
         return fail(SGEMM_ERR_SCRATCH,
-                    "sgemm_noalloc: %d K slices of a %lld x %lld result need %zu bytes of scratch; the fixed device "
-                    "array holds %zu bytes",
-                    pl.split_k, (long long)m, (long long)n, need, kNoAllocScratchBytes);
+                    "sgemm_noalloc: %d K slices of a %lld x %lld result (%.0f bytes of partial sums) do not fit the "
+                    "fixed device array of %zu bytes",
+                    pl.split_k, (long long)m, (long long)n, 4.0 * pl.split_k * static_cast<double>(ldp * n),
+                    kNoAllocScratchBytes);
     float* scratch = nullptr;
     if ((rc = noalloc_scratch(dev, &scratch))) return rc;
 
@@ -941,6 +989,55 @@ PG_EXPORT int sgemm_noalloc(char transa, char transb, int64_t m, int64_t n, int6
     if (m == 0 || n == 0 || ((k == 0 || alpha == 0.0f) && beta == 1.0f)) return 0;  // C unchanged
     return run_noalloc(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode,
                        static_cast<cudaStream_t>(stream));
+}
+
+PG_EXPORT int sgemm_set_workspace(void* workspace, size_t bytes, void* stream) {
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(-1, "argument 1 (workspace): %p is not 256-byte aligned", workspace);
+    if (workspace == nullptr && bytes != 0)
+        return fail(-2, "argument 2 (bytes): must be 0 when the workspace is null (null restores the library's own)");
+    int dev;
+    DeviceState* ds;
+    int rc = current_device(&dev, &ds);
+    if (rc) return rc;
+    cudaError_t e;
+    if (workspace != nullptr) {
+        cudaPointerAttributes at{};
+        if ((e = cudaPointerGetAttributes(&at, workspace)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(-1, "argument 1 (workspace): %p is not memory the CUDA runtime knows (%s)", workspace,
+                        cudaGetErrorString(e));
+        }
+        if (!((at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev))
+            return fail(-1, "argument 1 (workspace): %p is not device memory of the current device %d", workspace,
+                        dev);
+        uintptr_t base = 0;
+        size_t size = 0;
+        if (allocation_range(workspace, &base, &size) &&
+            (bytes > size || reinterpret_cast<uintptr_t>(workspace) - base > size - bytes))
+            return fail(-2, "argument 2 (bytes): %zu bytes from %p run past the end of its allocation", bytes,
+                        workspace);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const std::pair<int, uintptr_t> key{dev, reinterpret_cast<uintptr_t>(st)};
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (workspace == nullptr) {
+        g_user_ws.erase(key);
+        return 0;
+    }
+    // The library's own workspace for this stream is no longer used: free it in
+    // stream order (after the work already queued that may still use it).
+    auto it = g_bufs.find({key, kPurposeWorkspace});
+    if (it != g_bufs.end() && it->second.ptr != nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((e = cudaStreamIsCapturing(st, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(SGEMM_ERR_CAPTURE, "sgemm_set_workspace would free the stream's workspace during capture");
+        if ((e = cudaFreeAsync(it->second.ptr, st)) != cudaSuccess) return fail_cuda(e, "cudaFreeAsync(workspace)");
+        g_bufs.erase(it);
+    }
+    g_user_ws[key] = Buf{workspace, bytes};
+    return 0;
 }
 
 PG_EXPORT int sgemm_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,

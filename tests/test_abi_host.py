@@ -293,8 +293,8 @@ def test_plan_struct_layout_matches_header(lib, tmp_path):
 def test_plain_c_caller_links_and_calls_the_library(lib, tmp_path):
     """A C program with no Python or torch in it links the shared library and
     calls it through the header alone: the version, the planner on a device it
-    does not touch, an invalid argument answered with -i and a message, and a
-    call with nothing to do."""
+    does not touch, an invalid argument answered with -i and a message, a call
+    with nothing to do, and the workspace setter's argument checks."""
     src = tmp_path / "caller.c"
     src.write_text(r'''
 #include <stdio.h>
@@ -320,6 +320,9 @@ int main(void) {
                    (const void *)16384, 64, SGEMM_FFMA, 0, &p) != -15) return 11;
     if (sgemm_plan('N', 'N', 64, 48, 32, 1.0f, (const void *)4096, 64, (const void *)8192, 32, 0.0f,
                    (const void *)16384, 64, SGEMM_FFMA, 152, NULL) != -16) return 12;
+    if (sgemm_set_workspace((void *)4112, 64, NULL) != -1) return 13;
+    if (!strstr(sgemm_last_error_string(), "argument 1")) return 14;
+    if (sgemm_set_workspace(NULL, 64, NULL) != -2) return 15;
     puts("ok");
     return 0;
 }
