@@ -53,6 +53,14 @@ WORKLOADS = {
 
 # Nominal ratio of dense TF32 to dense BF16 tensor throughput (1.1 / 2.25 PFLOP/s).
 TF32_PER_BF16 = 1.1 / 2.25
+# TF32 flops per clock per SM of tcgen05 (2048 FMA): the register/TMEM-only probe
+# (probes/tf32_ceiling.cu, `bench.py --tf32-ceiling`) measured 4090 on GB300.
+TF32_FLOPS_PER_CLK_SM = 4096
+# The acceptance workloads timed after the headline step, one entry each (the
+# 8192^3 product is the headline itself).
+SWEEP = ("c1_256", "c2_rm1024", "c2_rm2048", "c2_rm4096", "c3_ragged", "c4_16384", "c5a_16384x16384x64",
+         "c5b_128x128x262144", "c5c_8192x64x8192")
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
 
 
@@ -69,6 +77,41 @@ def measured_peaks():
 def fp32_alu_peak_tflops(num_sms: int, mhz: float) -> float:
     """CUDA-core FP32 FMA peak: SMs x 128 FP32 lanes x 2 flops x clock."""
     return num_sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def tensor_pipe_tflops(num_sms: int, mhz: float) -> float:
+    """TF32 tensor-pipe peak: SMs x 4096 flops/clk (measured by the probe) x clock."""
+    return num_sms * TF32_FLOPS_PER_CLK_SM * mhz * 1e6 / 1e12
+
+
+def alg_bytes(p) -> int:
+    """A and B read once, C written, C read when beta != 0 (4 B each)."""
+    return (p.m * p.k + p.k * p.n + p.m * p.n * (2 if p.beta != 0 else 1)) * 4
+
+
+def make_config(wl_name: str, p, modes, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (identical keys and values)."""
+    desc = WORKLOADS[wl_name][0]
+    return {"workload": desc, "name": wl_name, "m": p.m, "n": p.n, "k": p.k, "modes": list(modes),
+            "layout": p.layout, "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (no flush)" if alg_bytes(p) > 129e6 else "L2 not flushed; inputs fit"}
+
+
+def mode_figures(mode: str, p, ms: float, peaks: dict) -> dict:
+    """TFLOP/s of one call and its fractions: of the mode's compute peak, of the
+    roofline min(compute peak, AI x HBM), and (tensor-core modes) of the TF32
+    tensor pipe at the maximum SM clock, counting 3xTF32's three products."""
+    flops = p.flops()
+    tflops = flops / (ms * 1e-3) / 1e12
+    compute = {"ffma": peaks["fp32"], "tf32": peaks["tf32"], "3xtf32": peaks["tf32"] / 3.0}[mode]
+    hbm_roof = (flops / alg_bytes(p)) * peaks["hbm"] / 1e3  # AI [flop/B] x HBM [GB/s] -> TFLOP/s
+    roof = min(compute, hbm_roof)
+    out = {"ms_median": ms, "tflops": tflops, "compute_peak_tflops": compute,
+           "frac_of_compute_peak": tflops / compute, "bound": "hbm" if hbm_roof < compute else "compute",
+           "roofline_tflops": roof, "frac_of_roofline": tflops / roof}
+    if mode != "ffma":
+        out["frac_of_tensor_pipe"] = tflops * (3 if mode == "3xtf32" else 1) / peaks["pipe"]
+    return out
 
 
 # ----------------------------------------------------------------- clocks
@@ -251,18 +294,18 @@ def run_ours(args, wl_name):
     fp32_peak = fp32_alu_peak_tflops(num_sms, sm_max)
     tf32_peak = float(peaks.get("bf16_tflops") or FALLBACK["bf16_tflops"]) * TF32_PER_BF16
     hbm = float(peaks.get("hbm_gbs") or FALLBACK["hbm_gbs"])
-    alg_bytes = (p.m * p.k + p.k * p.n + p.m * p.n * (2 if p.beta != 0 else 1)) * 4
+    pk = {"fp32": fp32_peak, "tf32": tf32_peak, "hbm": hbm, "pipe": tensor_pipe_tflops(num_sms, sm_max)}
     mode_info = {}
     for m in modes:
         ms = statistics.median(per_mode_ms[m])
-        tflops = flops / (ms * 1e-3) / 1e12
-        compute_peak = {"ffma": fp32_peak, "tf32": tf32_peak, "3xtf32": tf32_peak / 3.0}[m]
-        roof = min(compute_peak, (flops / alg_bytes) * hbm / 1e3)  # AI [flop/B] x HBM [GB/s] -> TFLOP/s
-        mode_info[m] = {"ms_median": ms, "ms_min": min(per_mode_ms[m]), "tflops": tflops,
-                        "compute_peak_tflops": compute_peak, "frac_of_compute_peak": tflops / compute_peak,
-                        "roofline_tflops": roof, "frac_of_roofline": tflops / roof}
+        mode_info[m] = mode_figures(m, p, ms, pk)
+        mode_info[m]["ms_min"] = min(per_mode_ms[m])
+        tflops = mode_info[m]["tflops"]
         if clk and clk.get("sm_mhz") and m == "ffma":
             mode_info[m]["frac_of_peak_at_run_clock"] = tflops / fp32_alu_peak_tflops(num_sms, clk["sm_mhz"])
+        if clk and clk.get("sm_mhz") and m != "ffma":
+            mode_info[m]["frac_of_tensor_pipe_at_run_clock"] = (
+                tflops * (3 if m == "3xtf32" else 1) / tensor_pipe_tflops(num_sms, clk["sm_mhz"]))
 
     # Dominant kernel: the mode whose launches take longest in the step.
     dom = max(modes, key=lambda m: mode_info[m]["ms_median"])
@@ -284,23 +327,79 @@ def run_ours(args, wl_name):
     roofline["kernel"] = dom_kernel
     roofline["traffic"] = traffic
 
+    sweep = None
+    if not args.no_sweep and world == 1:  # per-workload timings: single-GPU runs only
+        # the headline step's buffers are no longer needed
+        del dA, dB, dC0, dC
+        torch.cuda.empty_cache()
+        sweep = run_sweep(args, modes, pk, stream)
+
     value = world * flops * len(modes) / (total_ms / args.steps * 1e-3) / 1e12
     line = {
         "metric": "SGEMM TFLOPS (2MNK/s) at 4096^3/8192^3 fp32; % of FP32 & TF32 peak",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded CPU draws: A, B and C_in in storage order, padding set to NaN)",
-        "config": {"workload": desc, "name": wl_name, "m": p.m, "n": p.n, "k": p.k, "modes": modes,
-                   "layout": p.layout, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (no flush)" if alg_bytes > 129e6 else "L2 not flushed; inputs fit"},
+        "config": make_config(wl_name, p, modes, world),
         "modes": mode_info, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
         "device_status": status, "clocks": clk, "gpu": torch.cuda.get_device_name(local), "sms": num_sms,
+        "tensor_pipe_peak": {"tflops": pk["pipe"], "source": "%d SMs x %d TF32 flops/clk/SM (probe-measured) x "
+                                                             "%.0f MHz" % (num_sms, TF32_FLOPS_PER_CLK_SM, sm_max)},
     }
+    if sweep is not None:
+        line["workloads"] = sweep
     if not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds, args.cpu_threads)
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def run_sweep(args, modes, pk, stream):
+    """Every acceptance workload besides the headline: per mode, W warm-up calls
+    and a few timed calls (CUDA events on the launching stream around each call),
+    with L2 flushed before each timed call by writing a 512 MiB buffer outside
+    the timed interval.  Returns {name: entry}."""
+    import precision_gemm_gb300 as pg
+    cfg = synth.config_problems()
+    reps = max(3, min(args.steps, args.sweep_reps))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    out = {}
+    for name in SWEEP:
+        p = cfg[name]
+        A, B, C = synth.make(p)
+        dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+
+        def call(mode):
+            if p.layout == "col":
+                pg.sgemm(p.transa, p.transb, p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode,
+                         stream)
+            else:
+                pg.sgemm_rm(p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, stream)
+        entry = {"m": p.m, "n": p.n, "k": p.k, "layout": p.layout, "alpha": p.alpha, "beta": p.beta,
+                 "lda": p.lda, "ldb": p.ldb, "ldc": p.ldc, "dist": p.dist, "reps": reps,
+                 "l2": "flushed before each timed call (512 MiB write)", "modes": {}}
+        for mode in modes:
+            for _ in range(args.warmup):
+                call(mode)
+            times = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(mode)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            entry["modes"][mode] = mode_figures(mode, p, statistics.median(times), pk)
+            entry["modes"][mode]["ms_min"] = min(times)
+        out[name] = entry
+        del dA, dB, dC
+    del flush
+    torch.cuda.empty_cache()
+    if pg.device_status() != 0:
+        raise RuntimeError("a kernel reported a failed bounded wait during the workload sweep")
+    return out
 
 
 def read_traffic(mode: str, kname: str, wl_name: str):
@@ -392,7 +491,8 @@ def run_reference(args, wl_name):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, same buffers as the GPU arm)",
-            "config": {"workload": desc, "name": wl_name, "m": p.m, "n": p.n, "k": p.k},
+            "config": make_config(wl_name, p, [m for m in args.modes.split(",") if m],
+                                  int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -410,6 +510,9 @@ def main():
     ap.add_argument("--cpu-threads", type=int, default=0)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload timings of the other acceptance configs")
+    ap.add_argument("--sweep-reps", type=int, default=5, help="timed calls per mode and workload in the sweep")
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="reference arm: CPU seconds per step (default: the run bounded to ~150 s)")
     ap.add_argument("--fma-ceiling", action="store_true",

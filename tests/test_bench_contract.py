@@ -38,6 +38,11 @@ def test_reference_arm_prints_one_contract_line():
     assert line["n_gpus"] == 1 and line["vs_baseline"] is None
     cfg = line["config"]
     assert (cfg["m"], cfg["n"], cfg["k"]) == (3000, 1500, 777) and "3000x1500x777" in cfg["workload"]
+    # the GPU arm builds its config with the same function and arguments: same keys, same values
+    sys.path.insert(0, ROOT)
+    import bench
+    ours = bench.make_config("ragged", bench.WORKLOADS["ragged"][1], ["ffma", "tf32", "3xtf32"], 1)
+    assert cfg == ours
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == line["value"] and cb["sample"]
     assert cb["unit"] == line["unit"]
