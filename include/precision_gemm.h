@@ -58,6 +58,13 @@ extern "C" {
 #define SGEMM_3XTF32 2 /* tensor cores, each operand split x = big + small (both
                           TF32); small*big + big*small + big*big accumulated in
                           FP32, which recovers FP32-level accuracy               */
+/* Subnormal operands: SGEMM_FFMA keeps them (no flush to zero).  The two
+ * tensor-core modes read every operand (3xTF32: each of its two parts) in TF32,
+ * whose 10 mantissa-field bits hold a subnormal only down to 2^-136: operand
+ * values below 2^-137 in magnitude act as zero there (so infinity times such a
+ * value gives NaN), and 3xTF32 keeps FP32-level accuracy for operands of
+ * magnitude 2^-118 and above.  The tensor core itself does not flush subnormal
+ * TF32 operands or FP32 sums. */
 
 /* Status codes. */
 #define SGEMM_SUCCESS 0

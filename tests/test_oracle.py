@@ -293,6 +293,35 @@ def test_checker_flags_errors():
     assert not oracle.check(np.array([1.0, np.nan]), r, np.array([np.inf, np.nan]), 1e-5)["ok"]
 
 
+def test_checker_floor_covers_fp32_underflow(oracle_lib):
+    """Why the check has an absolute floor: FP32 with gradual underflow rounds a
+    result below 2^-126 to a multiple of 2^-149, so a dot product whose products
+    underflow carries an absolute error no relative bound covers.  Modelled here
+    on the CPU: a sequential FP32 fused multiply-add loop (the product and the
+    running sum added exactly in double, then rounded once to float32, which
+    keeps subnormals) over k products near 2^-144 misses tol * den, and stays
+    within tol * den + (k + 2) * 2^-149."""
+    rng = np.random.default_rng(3)
+    k = 512
+    a = (rng.uniform(1.0, 2.0, k) * np.where(rng.random(k) < 0.5, -1.0, 1.0) * 2.0 ** -72).astype(np.float32)
+    b = (rng.uniform(1.0, 2.0, k) * 2.0 ** -72).astype(np.float32)
+    acc = np.float32(0.0)
+    for p in range(k):
+        acc = np.float32(np.float64(acc) + np.float64(a[p]) * np.float64(b[p]))
+    assert 0 < abs(float(acc)) < 2.0 ** -126
+    A = torch.from_numpy(a.copy())            # 1 x k, lda 1
+    B = torch.from_numpy(b.copy())            # k x 1, ldb k
+    C = torch.zeros(1)
+    cref, den = oracle_lib.full("N", "N", 1, 1, k, 1.0, A, 1, B, k, 0.0, C, 1)
+    out = np.array([[float(acc)]])
+    assert not oracle.check(out, cref, den, 1e-5)["ok"]
+    assert oracle.check(out, cref, den, 1e-5, floor=(k + 2) * 2.0 ** -149)["ok"]
+    # the floor is a bound, not a pass for anything: an error of 10x the floor fails
+    assert not oracle.check(out + 10 * (k + 2) * 2.0 ** -149, cref, den, 1e-5, floor=(k + 2) * 2.0 ** -149)["ok"]
+    # and with floor = 0 the check is the plain normalised criterion
+    assert np.array_equal(oracle.normalised_error(out, cref, den), oracle.normalised_error(out, cref, den, 0.0))
+
+
 def test_synth_draws_are_seeded_and_padded():
     p = synth.Problem(5, 4, 3, lda=8, ldb=3, ldc=6, dist="normal", seed=42)
     A1, B1, C1 = synth.make(p)

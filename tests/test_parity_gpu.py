@@ -315,6 +315,64 @@ def test_special_values_match_in_kind(mode, mnk):
     assert res["ok"], res
 
 
+TF32_SUBNORMAL_ZERO = 2.0 ** -137  # below this, a TF32 operand part reads as zero
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mnk", [(256, 64, 512), (512, 512, 1024), (128, 128, 4096)])
+def test_subnormal_operands(mode, mnk):
+    """Subnormal operands and products that underflow, on the single-SM kernel
+    (256 x 64, 128 x 128) and on SM pairs (512 x 512):
+      rows 0-7 of A   subnormals that TF32 holds exactly (j * 2^-136, j < 1024)
+      rows 8-15       subnormals below 2^-137 (j * 2^-149, j < 4096)
+      rows 16-23      normal values in [2^-117, 2^-116): 3xTF32 remainders subnormal
+      rows 24-31      2^-70 scale, times columns 0-7 of B at 2^-70: products underflow
+      cols 8-11 of B  TF32-exact subnormals; col 12 below 2^-137
+      A(40, 3) = inf, met by B(3, 8) (a subnormal) and B(3, 12) (below 2^-137).
+    FFMA is held to the oracle on these inputs.  The tensor-core modes read each
+    operand (3xTF32: each of its two parts) in TF32, whose 10 mantissa-field bits
+    hold a subnormal only to 2^-136: the tensor core does not flush what TF32
+    holds (rows 0-7 and cols 8-11 are exact), values below 2^-137 read as zero,
+    and 3xTF32 keeps 1e-5 for operands from 2^-118 up.  So they are held to the
+    oracle on the same inputs with the values below 2^-137 set to zero.  Every
+    check allows FP32's absolute underflow error, (k + 2) * 2^-149 per output."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, alpha=1.0, beta=0.0, dist="normal", seed=89)
+    A, B, C = synth.make(p)
+    g = torch.Generator().manual_seed(90)
+    a = A[: p.lda * k].view(k, p.lda)    # a[q, i] = A(i, q)
+    b = B[: p.ldb * n].view(n, p.ldb)    # b[j, q] = B(q, j)
+
+    def signs(*shape):
+        return torch.where(torch.rand(*shape, generator=g) < 0.5, -1.0, 1.0)
+
+    a[:, 0:8] = signs(k, 8) * torch.randint(1, 1024, (k, 8), generator=g).float() * 2.0 ** -136
+    a[:, 8:16] = signs(k, 8) * torch.randint(1, 4096, (k, 8), generator=g).float() * 2.0 ** -149
+    a[:, 16:24] = signs(k, 8) * (1.0 + torch.rand(k, 8, generator=g)) * 2.0 ** -117
+    a[:, 24:32] = signs(k, 8) * (1.0 + torch.rand(k, 8, generator=g)) * 2.0 ** -70
+    b[0:8, :] = signs(8, k) * (1.0 + torch.rand(8, k, generator=g)) * 2.0 ** -70
+    b[8:12, :] = signs(4, k) * torch.randint(1, 1024, (4, k), generator=g).float() * 2.0 ** -136
+    b[12, :] = signs(k) * torch.randint(1, 4096, (k,), generator=g).float() * 2.0 ** -149
+    a[3, 40] = float("inf")
+    assert bool((a[:, 8:16].abs() < TF32_SUBNORMAL_ZERO).all()) and bool((b[12].abs() < TF32_SUBNORMAL_ZERO).all())
+    out, ok = H.run_gpu(p, mode, A, B, C)
+    assert ok
+    got = H.logical(p, out)
+    if mode == "ffma":
+        Ar, Br = A, B
+    else:
+        tiny = lambda t: (t.abs() < TF32_SUBNORMAL_ZERO) & (t != 0)  # noqa: E731
+        Ar = torch.where(tiny(A), torch.zeros_like(A), A)
+        Br = torch.where(tiny(B), torch.zeros_like(B), B)
+    cref, den = H.reference_full(p, Ar, Br, C)
+    res = oracle.check(got, cref, den, oracle.TOL[mode], floor=(k + 2) * 2.0 ** -149)
+    assert res["ok"], res
+    # the inputs did reach the cases: underflowing products, and a non-zero TF32-exact subnormal product
+    assert 0 < np.abs(cref[24:32, 0:8]).max() < 2.0 ** -126
+    assert np.isinf(cref[40, 8]) and np.isinf(got[40, 8])
+    assert np.all(got[0:8, 13:20] != 0)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_beta_zero_ignores_nan_c(mode):
     p = synth.Problem(200, 150, 100, alpha=1.0, beta=0.0, dist="normal", seed=17)
