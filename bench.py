@@ -319,9 +319,9 @@ def run_ours(args, wl_name):
                     "peak_source": "derived: %d SMs x 128 FP32 lanes x 2 x %.0f MHz (%s max SM clock)"
                                    % (num_sms, sm_max, peak_src)}
     else:
-        pk = tf32_peak if dom == "tf32" else tf32_peak / 3.0
-        roofline = {"bound": "tensor", "achieved": mode_info[dom]["tflops"], "peak": pk, "unit": "TFLOP/s",
-                    "frac": mode_info[dom]["tflops"] / pk,
+        dom_peak = tf32_peak if dom == "tf32" else tf32_peak / 3.0
+        roofline = {"bound": "tensor", "achieved": mode_info[dom]["tflops"], "peak": dom_peak, "unit": "TFLOP/s",
+                    "frac": mode_info[dom]["tflops"] / dom_peak,
                     "peak_source": "%s bf16 burst x %.3f (nominal tf32/bf16)%s" % (
                         peak_src, TF32_PER_BF16, " / 3" if dom == "3xtf32" else "")}
     roofline["kernel"] = dom_kernel
