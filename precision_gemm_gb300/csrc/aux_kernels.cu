@@ -104,6 +104,65 @@ __global__ void __launch_bounds__(256, SPLIT ? 3 : 4)
         });
 }
 
+// prep_copy_kernel for a 16-byte aligned src with lds % 4 == 0 (dst is 256-byte
+// aligned with ldd = round_up(rows, 4)): a thread moves 4 consecutive rows of one
+// column as one float4, kU chunks loaded before any is stored, so that small
+// operands (a few MB, where the scalar sweep is bound by DRAM latency) move with
+// many loads in flight.  A column's last chunk, when rows % 4 != 0, is read and
+// written element by element.
+template <bool SPLIT>
+__global__ void __launch_bounds__(256) prep_copy_vec_kernel(const float* __restrict__ src, int64_t lds, int64_t rows,
+                                                            int64_t cols, float* __restrict__ dst,
+                                                            float* __restrict__ dst_small, int64_t ldd) {
+    const int64_t rq = (rows + 3) / 4;  // chunks per column
+    const int64_t total = rq * cols;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t0 < total; t0 += kU * stride) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t t = t0 + u * stride;
+            if (t < total) {
+                const int64_t c = t / rq, r = (t - c * rq) * 4;
+                const float* s = src + c * lds + r;
+                if (r + 4 <= rows) {
+                    v[u] = *reinterpret_cast<const float4*>(s);
+                } else {
+                    v[u] = make_float4(s[0], r + 1 < rows ? s[1] : 0.0f, r + 2 < rows ? s[2] : 0.0f, 0.0f);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t t = t0 + u * stride;
+            if (t < total) {
+                const int64_t c = t / rq, r = (t - c * rq) * 4;
+                const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                float b[4], sm[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (SPLIT) {
+                        split_tf32(x[e], b[e], sm[e]);
+                    } else {
+                        b[e] = x[e];
+                    }
+                }
+                float* d = dst + c * ldd + r;
+                float* ds = SPLIT ? dst_small + c * ldd + r : nullptr;
+                if (r + 4 <= rows) {
+                    *reinterpret_cast<float4*>(d) = make_float4(b[0], b[1], b[2], b[3]);
+                    if (SPLIT) *reinterpret_cast<float4*>(ds) = make_float4(sm[0], sm[1], sm[2], sm[3]);
+                } else {
+                    for (int e = 0; e < 4 && r + e < rows; ++e) {
+                        d[e] = b[e];
+                        if (SPLIT) ds[e] = sm[e];
+                    }
+                }
+            }
+        }
+    }
+}
+
 // dst(r, c) = src(c, r): 32 x 32 tiles through shared memory so that both the
 // read (along c) and the write (along r) are coalesced.
 template <bool SPLIT>
@@ -141,32 +200,66 @@ __global__ void __launch_bounds__(256) prep_transpose_kernel(const float* __rest
     }
 }
 
-// C = alpha * sum_{s < split} P[s] + beta * C over the m x n output; every
-// output sums its slices in increasing s.  Loads run kS slices ahead of the
-// additions, so kS loads are in flight per output even when a thread owns one.
+// Loads of the split-K reductions run up to kS slices ahead of the additions.
 constexpr int kS = 8;
 
-__global__ void __launch_bounds__(256, 4) splitk_reduce_kernel(const GemmParams p, int tx_shift) {
-    const Sweep w = sweep_setup(tx_shift);
-    const float* __restrict__ P = p.P;
-    float* __restrict__ C = p.C;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * w.TX + w.tx; r < p.m; r += w.rstep) {
-        for (int64_t c = static_cast<int64_t>(blockIdx.y) * w.TY + w.ty; c < p.n; c += w.cstep) {
-            const float* ps = P + c * p.ldp + r;
-            const float cin = p.beta != 0.0f ? C[c * p.ldc + r] : 0.0f;
-            float acc = 0.0f;
-            int s = 0;
-            for (; s + kS <= p.split; s += kS) {
-                float v[kS];
-#pragma unroll
-                for (int j = 0; j < kS; ++j) v[j] = ps[(s + j) * p.p_stride];
-#pragma unroll
-                for (int j = 0; j < kS; ++j) acc += v[j];
+// C = alpha * sum_{s < split} P[s] + beta * C over the m x n output, every output
+// summing its slices in increasing s.  A thread takes 4 consecutive rows of one
+// column.  The slices' float4s of P (16-byte aligned: ldp % 4 == 0 and P starts
+// on 256 bytes) are loaded before the first addition -- up to kS per batch -- so
+// that even a thread with one output keeps several loads in flight.  C is read
+// and written as a float4 when it is 16-byte aligned with ldc % 4 == 0 and the
+// chunk is whole, else element by element.  Rows from m up to ldp of P are
+// loaded with the chunk but never stored.
+__global__ void __launch_bounds__(256) splitk_reduce_vec_kernel(const GemmParams p) {
+    const int64_t rq = (p.m + 3) / 4;
+    const int64_t total = rq * p.n;
+    const int64_t st4 = p.p_stride / 4;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t c = t / rq, r = (t - c * rq) * 4;
+        const float4* ps = reinterpret_cast<const float4*>(p.P + c * p.ldp + r);
+        float* dst = p.C + c * p.ldc + r;
+        const bool whole = r + 4 <= p.m;
+        const bool vec = whole && p.c_vec;
+        float4 cin = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (p.beta != 0.0f) {
+            if (vec) {
+                cin = *reinterpret_cast<const float4*>(dst);
+            } else {
+                cin.x = dst[0];
+                if (r + 1 < p.m) cin.y = dst[1];
+                if (r + 2 < p.m) cin.z = dst[2];
+                if (r + 3 < p.m) cin.w = dst[3];
             }
-            for (; s < p.split; ++s) acc += ps[s * p.p_stride];
-            float o = p.alpha * acc;
-            if (p.beta != 0.0f) o = fmaf(p.beta, cin, o);
-            C[c * p.ldc + r] = o;
+        }
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s = 0; s < p.split; s += kS) {
+            float4 v[kS];
+#pragma unroll
+            for (int j = 0; j < kS; ++j)
+                if (s + j < p.split) v[j] = ps[(s + j) * st4];
+#pragma unroll
+            for (int j = 0; j < kS; ++j) {
+                if (s + j < p.split) {
+                    acc.x += v[j].x;
+                    acc.y += v[j].y;
+                    acc.z += v[j].z;
+                    acc.w += v[j].w;
+                }
+            }
+        }
+        float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+        if (p.beta != 0.0f) {
+            o[0] = fmaf(p.beta, cin.x, o[0]);
+            o[1] = fmaf(p.beta, cin.y, o[1]);
+            o[2] = fmaf(p.beta, cin.z, o[2]);
+            o[3] = fmaf(p.beta, cin.w, o[3]);
+        }
+        if (vec) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            for (int e = 0; e < 4 && r + e < p.m; ++e) dst[e] = o[e];
         }
     }
 }
@@ -269,6 +362,19 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
         else
             prep_transpose_kernel<false><<<static_cast<unsigned>(g), block, 0, stream>>>(src, lds, rows, cols,
                                                                                          dst, nullptr, ldd);
+    } else if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && lds % 4 == 0 &&
+               (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && ldd % 4 == 0 &&
+               (dst_small == nullptr || (reinterpret_cast<uintptr_t>(dst_small) & 15u) == 0)) {
+        const int64_t chunks = (rows + 3) / 4 * cols;
+        int64_t g = (chunks + 255) / 256;
+        const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+        if (g > cap) g = cap;
+        if (dst_small)
+            prep_copy_vec_kernel<true><<<static_cast<unsigned>(g), 256, 0, stream>>>(src, lds, rows, cols, dst,
+                                                                                    dst_small, ldd);
+        else
+            prep_copy_vec_kernel<false><<<static_cast<unsigned>(g), 256, 0, stream>>>(src, lds, rows, cols, dst,
+                                                                                     nullptr, ldd);
     } else {
         int sh = 8, by_rows = 0;
         const dim3 grid = sweep_grid(rows, cols, num_sms, &sh, &by_rows);
@@ -293,9 +399,13 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t 
             p);
         return cudaGetLastError();
     }
-    int sh = 8, by_rows = 0;
-    const dim3 grid = sweep_grid(p.m, p.n, num_sms, &sh, &by_rows);
-    splitk_reduce_kernel<<<grid, 256, 0, stream>>>(p, sh);
+    // the partial sums' layout: ldp a multiple of 4, P 16-byte aligned (the workspace regions start on 256 bytes)
+    if (p.ldp % 4 != 0 || (reinterpret_cast<uintptr_t>(p.P) & 15u) != 0) return cudaErrorInvalidValue;
+    const int64_t chunks = (p.m + 3) / 4 * p.n;
+    int64_t g = (chunks + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+    if (g > cap) g = cap;
+    splitk_reduce_vec_kernel<<<static_cast<unsigned>(g), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -414,6 +414,31 @@ def test_scale_sweep_shapes(shape):
 
 
 @pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("m,ldc", [(301, 304), (301, 303), (300, 300), (2, 8)])
+@pytest.mark.parametrize("split", [2, 3, 9])
+def test_splitk_reduce_rows_in_fours(mode, m, ldc, split):
+    """The split-K reduction takes 4 rows of a column per thread: whole and ragged
+    last chunks (m % 4 != 0), C read and written as float4 (16-byte aligned,
+    ldc % 4 == 0) or element by element, beta != 0, and more slices than one
+    batch of loads (9 > 8); bitwise repeatable."""
+    p = synth.Problem(m, 77, 864, lda=m + 1, ldc=ldc, alpha=-0.75, beta=1.25, dist="normal", seed=97)  # 27 k-blocks
+    A, B, C = synth.make(p)
+    try:
+        pg.force_plan(0, split)
+        plan = pg.sgemm_plan("N", "N", p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode)
+        assert plan["split_k"] == split, plan
+        out1, ok1 = H.run_gpu(p, mode, A, B, C)
+        out2, ok2 = H.run_gpu(p, mode, A, B, C)
+    finally:
+        pg.force_plan(0, 0)
+    assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, out1), cref, den, oracle.TOL[mode])
+    assert res["ok"], res
+    assert H.padding_intact(p, out1, C)
+
+
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(96, 3, 50000), (5000, 3, 70), (130, 130, 100000)])
 def test_split_prep_and_reduce_shapes(mode, mnk):
     """Operand copies / TF32 splits of tall-narrow and short-wide operands, and
