@@ -249,8 +249,10 @@ typedef struct sgemm_plan {
     size_t smem_bytes;       /* dynamic shared memory of the GEMM kernel        */
     size_t workspace_bytes;  /* device workspace the call needs                 */
     int launches;            /* kernels the call launches                       */
-    int tail_tiles;          /* SM pairs: last-wave tiles whose K is split ...  */
+    int tail_tiles;          /* SM pairs and FFMA: last-wave tiles whose K is split ... */
     int tail_split;          /* ... into this many slices (1: none)             */
+    int sk_ctas;             /* FFMA stream-K: CTAs sharing all (tile, k-block)
+                                iterations in equal ranges (0: not used)        */
 } sgemm_plan_t;
 
 /*

@@ -65,7 +65,7 @@ class sgemm_plan_t(ctypes.Structure):
         "tiles_m", "tiles_n", "prep_a", "prep_b", "threads", "ctas_per_sm")] + [
         ("ld_a", ctypes.c_int64), ("ld_b", ctypes.c_int64), ("smem_bytes", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t), ("launches", ctypes.c_int), ("tail_tiles", ctypes.c_int),
-        ("tail_split", ctypes.c_int)]
+        ("tail_split", ctypes.c_int), ("sk_ctas", ctypes.c_int)]
 
 
 _lib = None

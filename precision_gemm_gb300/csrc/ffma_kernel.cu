@@ -74,6 +74,39 @@ struct FfmaCfg {
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128B-swizzle slots need 1 KiB alignment");
 };
 
+// One k-block of the thread's 8 x JJ register tile from the ring slot at `slot`
+// (the stream-K kernel's form of the data-parallel kernel's inner loop): per
+// pair of k values JJ float2 of B (two k values of one column each), per k 2
+// float4 of A, then the packed two-lane FMAs.
+template <int BN, int JJ>
+__device__ __forceinline__ void ffma_kblock(float2 (&acc)[4][JJ], const uint8_t* slot, int tm, int tn,
+                                            uint32_t bchunk_xor) {
+    using Cfg = FfmaCfg<BN, JJ>;
+    const float* As = reinterpret_cast<const float*>(slot);
+    const uint8_t* Bs = slot + Cfg::A_BYTES + tn * 128;
+#pragma unroll
+    for (int g2 = 0; g2 < Cfg::BK / 2; ++g2) {
+        float2 b[JJ];
+        const uint32_t off2 = (((static_cast<uint32_t>(g2 >> 1)) ^ bchunk_xor) << 4) + ((g2 & 1) << 3);
+#pragma unroll
+        for (int jj = 0; jj < JJ; ++jj) b[jj] = *reinterpret_cast<const float2*>(Bs + jj * (Cfg::TGN * 128) + off2);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const float* arow = As + (2 * g2 + kk) * Cfg::BM;
+            const float4 a0 = *reinterpret_cast<const float4*>(arow + 4 * tm);
+            const float4 a1 = *reinterpret_cast<const float4*>(arow + 64 + 4 * tm);
+            const float2 a[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                                 make_float2(a1.z, a1.w)};
+#pragma unroll
+            for (int jj = 0; jj < JJ; ++jj) {
+                const float bv = kk == 0 ? b[jj].x : b[jj].y;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r][jj] = __ffma2_rn(a[r], make_float2(bv, bv), acc[r][jj]);
+            }
+        }
+    }
+}
+
 template <int BN, int JJ>
 __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTAS_PER_SM)
     ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -328,6 +361,255 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
     }
 }
 
+// ---------------- stream-K ----------------
+//
+// For products whose tiles fill less than one wave of CTA slots (the pages'
+// "tail" share of the gap, "V3. Vectorized and double buffer", section 4),
+// every one of G co-resident CTAs takes the same share of all (tile, k-block)
+// iterations: CTA c runs the contiguous range [c T / G, (c + 1) T / G) of the
+// T = tiles x k-blocks iterations in tile-major order, crossing tile boundaries.
+// Its loader streams the whole range through the ring without a break; at the
+// end of each tile segment the consumers store the segment's accumulators as
+// a raw 128 x BN partial block and start the next segment from zero.  Segment j
+// of tile t (the j-th CTA touching t) goes to slot t * maxseg + j.  A second
+// kernel then adds each tile's partial blocks in segment order -- increasing k,
+// whichever CTA finished first, so the result is deterministic -- and applies
+// alpha and beta.
+
+// The CTA whose range holds iteration `it`: the largest c with c T / G <= it.
+__device__ __forceinline__ int sk_cta_of(int64_t it, int G, int64_t T) {
+    return static_cast<int>(((it + 1) * G - 1) / T);
+}
+
+// At most this many tile segments per CTA (the planner keeps to it).
+constexpr int kSkMaxSegs = 8;
+
+template <int BN, int JJ>
+__global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTAS_PER_SM)
+    ffma_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+    using Cfg = FfmaCfg<BN, JJ>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_smem_1024(smem_raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + S);
+    // This CTA's tile segments, built once by thread 0: tile, partial-block slot
+    // (t * maxseg + j), k-blocks, first k-block, and the tile's origin in C.
+    __shared__ int seg_slot[kSkMaxSegs], seg_len[kSkMaxSegs], seg_k0[kSkMaxSegs], seg_m0[kSkMaxSegs],
+        seg_n0[kSkMaxSegs];
+    __shared__ int n_segs, n_its, ld_seg, ld_kb;  // ld_*: the loader's position (thread 0 only)
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, Cfg::CWARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        const int G = gridDim.x, c = blockIdx.x;
+        const int64_t T = p.sk_iters;
+        const int kb = p.kb_total;
+        const int64_t it0 = static_cast<int64_t>(c) * T / G, it1 = static_cast<int64_t>(c + 1) * T / G;
+        int ns = 0;
+        for (int64_t it = it0; it < it1 && ns < kSkMaxSegs; ++ns) {
+            const int tile = static_cast<int>(it / kb);
+            const int k0 = static_cast<int>(it - static_cast<int64_t>(tile) * kb);
+            const int len = static_cast<int>(min(static_cast<int64_t>(kb - k0), it1 - it));
+            int tm_, tn_;
+            tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm_, tn_);
+            seg_slot[ns] = tile * p.sk_maxseg + (c - sk_cta_of(static_cast<int64_t>(tile) * kb, G, T));
+            seg_len[ns] = len;
+            seg_k0[ns] = k0;
+            seg_m0[ns] = tm_ * Cfg::BM;
+            seg_n0[ns] = tn_ * BN;
+            it += len;
+        }
+        n_segs = ns;
+        n_its = static_cast<int>(it1 - it0);
+        // The planner keeps every CTA within kSkMaxSegs segments; were the range
+        // longer, this CTA would leave part of it undone: report a failure
+        // instead of a wrong C.
+        int64_t covered = 0;
+        for (int q = 0; q < ns; ++q) covered += seg_len[q];
+        if (covered != it1 - it0) {
+            n_its = 0;
+            raise_abort(abort_flag, p.status);
+        }
+        ld_seg = 0;
+        ld_kb = 0;
+    }
+    __syncthreads();
+    const int n_it = n_its;
+
+    // Thread 0 is also the loader, PD k-blocks ahead of the consumers.
+    const bool loader = (threadIdx.x == 0) && !(p.debug_flags & 1);
+    int issued = 0;
+    auto issue = [&](int g) -> bool {
+        const int s = g % S;
+        if (!mbar_wait_bounded(empty0 + 8 * s, ((g / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            raise_abort(abort_flag, p.status);
+            return false;
+        }
+        const int sg = ld_seg, kq = ld_kb;
+        const uint32_t full = full0 + 8 * s;
+        mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+        const int32_t kc = (seg_k0[sg] + kq) * Cfg::BK;
+        const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES);
+        tma_load_2d(slot, &tmA, seg_m0[sg], kc, full);
+        tma_load_2d(slot + Cfg::A_BYTES, &tmB, kc, seg_n0[sg], full);
+        if (kq + 1 == seg_len[sg]) {
+            ld_seg = sg + 1;
+            ld_kb = 0;
+        } else {
+            ld_kb = kq + 1;
+        }
+        issued = g + 1;
+        return true;
+    };
+    if (loader) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int g = 0; g < min(Cfg::PD, n_it); ++g)
+            if (!issue(g)) break;
+    }
+
+    const int wm = warp & 3;
+    const int wn = warp >> 2;
+    const int tm = 4 * wm + (lane >> 3);
+    const int tn = 8 * wn + (lane & 7);
+    const uint32_t bchunk_xor = static_cast<uint32_t>(tn & 7);
+    float2 acc[4][JJ];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < JJ; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+
+    int seg = 0, left = seg_len[0];  // the segment being computed and its k-blocks still to come
+    for (int g = 0; g < n_it; ++g) {
+        const int s = g % S;
+        if (loader && issued == g + Cfg::PD && issued < n_it && !*abort_flag) issue(issued);
+        const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * s, (g / S) & 1, p.timeout_ns,
+                                                                       abort_flag));
+        if (!landed) {
+            if (lane == 0) raise_abort(abort_flag, p.status);
+            break;
+        }
+        ffma_kblock<BN, JJ>(acc, smem + s * Cfg::STAGE_BYTES, tm, tn, bchunk_xor);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (--left == 0) {  // the segment's last k-block: store its partial block, start the next from zero
+            float* part = p.sk_P + static_cast<int64_t>(seg_slot[seg]) * (Cfg::BM * BN) + 4 * tm;
+#pragma unroll
+            for (int jj = 0; jj < JJ; ++jj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    *reinterpret_cast<float4*>(part + (tn + Cfg::TGN * jj) * Cfg::BM + 64 * h) =
+                        make_float4(acc[2 * h][jj].x, acc[2 * h][jj].y, acc[2 * h + 1][jj].x, acc[2 * h + 1][jj].y);
+                    acc[2 * h][jj] = make_float2(0.0f, 0.0f);
+                    acc[2 * h + 1][jj] = make_float2(0.0f, 0.0f);
+                }
+            if (++seg < n_segs) left = seg_len[seg];
+        }
+    }
+    if (loader) {
+        for (int g = max(0, issued - S); g < issued; ++g)
+            mbar_wait_bounded(full0 + 8 * (g % S), (g / S) & 1, p.timeout_ns, nullptr);
+    }
+}
+
+// C = alpha * sum_j P[t][j] + beta * C per tile t, the segments j of t added in
+// increasing order.  A thread takes 4 consecutive rows of one column of a tile
+// (one float4 of each partial block), all of its segments' loads issued before
+// the additions; C is read and written as a float4 when it is 16-byte aligned
+// with ldc % 4 == 0 and the 4 rows lie inside C.
+template <int BN>
+__global__ void __launch_bounds__(256) ffma_sk_fixup_kernel(const GemmParams p, int G) {
+    constexpr int BM = kBM;
+    constexpr int RQ = BM / 4;       // float4 chunks per tile column
+    constexpr int CH = RQ * BN;      // per tile
+    constexpr int kMaxSeg = 8;       // loads in flight per batch
+    const int64_t T = p.sk_iters;
+    const int kb = p.kb_total;
+    const int64_t total = static_cast<int64_t>(p.tiles_m) * p.tiles_n * CH;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(q / CH);
+        const int r = static_cast<int>(q - static_cast<int64_t>(t) * CH);
+        const int col = r / RQ, row4 = (r - col * RQ) * 4;
+        int tmi, tni;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tmi, tni);
+        const int64_t i = static_cast<int64_t>(tmi) * BM + row4;
+        const int64_t jc = static_cast<int64_t>(tni) * BN + col;
+        if (i >= p.m || jc >= p.n) continue;
+        const int64_t first = static_cast<int64_t>(t) * kb;
+        const int nseg = sk_cta_of(first + kb - 1, G, T) - sk_cta_of(first, G, T) + 1;
+        const float4* src = reinterpret_cast<const float4*>(p.sk_P + static_cast<int64_t>(t) * p.sk_maxseg * (BM * BN) +
+                                                            col * BM + row4);
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int j0 = 0; j0 < nseg; j0 += kMaxSeg) {
+            float4 v[kMaxSeg];
+#pragma unroll
+            for (int u = 0; u < kMaxSeg; ++u)
+                if (j0 + u < nseg) v[u] = __ldcg(src + static_cast<int64_t>(j0 + u) * (BM * BN / 4));
+#pragma unroll
+            for (int u = 0; u < kMaxSeg; ++u) {
+                if (j0 + u < nseg) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
+            }
+        }
+        float* dst = p.C + jc * p.ldc + i;
+        const bool vec = p.c_vec && i + 3 < p.m;
+        float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+        if (p.beta != 0.0f) {
+            float cin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (vec) {
+                const float4 cv = *reinterpret_cast<const float4*>(dst);
+                cin[0] = cv.x;
+                cin[1] = cv.y;
+                cin[2] = cv.z;
+                cin[3] = cv.w;
+            } else {
+                for (int e = 0; e < 4 && i + e < p.m; ++e) cin[e] = dst[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = fmaf(p.beta, cin[e], o[e]);
+        }
+        if (vec) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            for (int e = 0; e < 4 && i + e < p.m; ++e) dst[e] = o[e];
+        }
+    }
+}
+
+template <int BN, int JJ>
+cudaError_t launch_sk_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int ctas,
+                           int num_sms, cudaStream_t stream) {
+    using Cfg = FfmaCfg<BN, JJ>;
+    auto kern = ffma_sk_kernel<BN, JJ>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::SMEM));
+    if (e != cudaSuccess) return e;
+    kern<<<ctas, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t chunks = static_cast<int64_t>(p.tiles_m) * p.tiles_n * (kBM / 4) * BN;
+    int64_t g = (chunks + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+    if (g > cap) g = cap;
+    ffma_sk_fixup_kernel<BN><<<static_cast<unsigned>(g), 256, 0, stream>>>(p, ctas);
+    return cudaGetLastError();
+}
+
 template <int BN, int JJ>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, dim3 grid,
                         cudaStream_t stream) {
@@ -352,6 +634,15 @@ int ffma_ctas_per_sm(int bn) {
     return bn == 64 ? Cfg64::CTAS_PER_SM : bn == 128 ? Cfg128::CTAS_PER_SM : Cfg256::CTAS_PER_SM;
 }
 size_t ffma_smem_bytes(int bn) { return bn == 64 ? Cfg64::SMEM : bn == 128 ? Cfg128::SMEM : Cfg256::SMEM; }
+
+cudaError_t launch_ffma_sk(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, int ctas,
+                           int num_sms, cudaStream_t stream) {
+    switch (bn) {
+        case 64: return launch_sk_impl<64, 8>(tmA, tmB, p, ctas, num_sms, stream);
+        case 128: return launch_sk_impl<128, PG_FFMA_JJ128>(tmA, tmB, p, ctas, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn,
                         dim3 grid, cudaStream_t stream) {

@@ -43,6 +43,12 @@ struct GemmParams {
     int32_t tail_kb;
     float* tail_P;
     int* tail_cnt;
+    // FFMA stream-K: the CTAs share the sk_iters = tiles x kb_total (tile,
+    // k-block) iterations in equal contiguous ranges; segment j of tile t stores
+    // its partial block at sk_P + (t * sk_maxseg + j) * BM * BN ([column][row]).
+    int64_t sk_iters;
+    int32_t sk_maxseg;
+    float* sk_P;
     uint64_t timeout_ns;     // limit of every bounded wait
     int* status;             // per-device status word
 };
@@ -59,6 +65,11 @@ int ffma_ctas_per_sm(int bn);
 size_t ffma_smem_bytes(int bn);
 cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
                         int bn, dim3 grid, cudaStream_t stream);
+// FFMA stream-K (bn in {64, 128}): `ctas` co-resident CTAs share the product's
+// (tile, k-block) iterations; then the fix-up kernel adds each tile's partial
+// blocks in order and applies alpha/beta.  Two launches.
+cudaError_t launch_ffma_sk(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int bn, int ctas,
+                           int num_sms, cudaStream_t stream);
 
 // tcgen05 kernel: tile 128 x bn, bn in {64, 128, 256}; split3 selects 3xTF32,
 // whose TF32 split this kernel does itself in shared memory (it serves the

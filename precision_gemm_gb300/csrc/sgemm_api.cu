@@ -41,6 +41,20 @@ namespace {
 #define PG_GROUP_M 16
 #endif
 
+// FFMA stream-K (a compile-time switch): products whose tiles fill less than
+// PG_FFMA_SK_FILL percent of one wave of CTA slots, even after a K split, with
+// at least 4 k-blocks per CTA, run on the stream-K kernel.
+#ifndef PG_FFMA_SK
+#define PG_FFMA_SK 1
+#endif
+#ifndef PG_FFMA_SK_FILL
+#define PG_FFMA_SK_FILL 90
+#endif
+#ifndef PG_FFMA_SK_MIN_KB
+#define PG_FFMA_SK_MIN_KB 32  // k-blocks per CTA at least
+#endif
+constexpr int kSkMaxSegsPerCta = 8;  // the kernel's segment table
+
 
 constexpr int kMaxDevices = 64;
 constexpr const char* kVersion = "precision_gemm_gb300 0.1.0 (sm_103a; FFMA, TF32, 3xTF32)";
@@ -102,6 +116,27 @@ int validate(char transa, char transb, int64_t m, int64_t n, int64_t k, float al
 }
 
 size_t region(int64_t elems) { return static_cast<size_t>(round_up(elems * 4, 256)); }
+
+// Stream-K: the CTA whose range [c T / G, (c + 1) T / G) holds iteration it, and
+// the most segments (CTAs) any tile is cut into -- the partial-block slots per tile.
+int64_t sk_cta_of(int64_t it, int64_t G, int64_t T) { return ((it + 1) * G - 1) / T; }
+// The most tiles (segments) any CTA's range touches.
+int sk_segs_per_cta(int64_t tiles, int64_t kb, int64_t G) {
+    const int64_t T = tiles * kb;
+    int64_t most = 0;
+    for (int64_t c = 0; c < G; ++c) {
+        const int64_t it0 = c * T / G, it1 = (c + 1) * T / G;
+        if (it1 > it0) most = std::max(most, (it1 - 1) / kb - it0 / kb + 1);
+    }
+    return static_cast<int>(most);
+}
+int sk_maxseg(int64_t tiles, int64_t kb, int64_t G) {
+    const int64_t T = tiles * kb;
+    int64_t most = 1;
+    for (int64_t t = 0; t < tiles; ++t)
+        most = std::max(most, sk_cta_of(t * kb + kb - 1, G, T) - sk_cta_of(t * kb, G, T) + 1);
+    return static_cast<int>(most);
+}
 
 // Workspace of the last-wave split: the partial blocks, and one arrival counter
 // per (tail tile, epilogue warp region).
@@ -250,8 +285,23 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
             split = std::min<int64_t>(capacity / tiles, pl->k_blocks / cdiv(min_k_slice, pl->bk));
     }
     split = std::max<int64_t>(1, std::min<int64_t>({split, static_cast<int64_t>(pl->k_blocks), 65535}));
-    const int64_t per = cdiv(pl->k_blocks, split);
+    int64_t per = cdiv(pl->k_blocks, split);
     split = cdiv(pl->k_blocks, per);  // no empty slice
+
+    // FFMA stream-K: when the tiles (times their K slices) leave more than a
+    // tenth of the wave's CTA slots idle, every slot takes an equal share of all
+    // (tile, k-block) iterations instead -- at least 32 k-blocks each, so that the
+    // partial blocks' round trip and the fix-up launch are repaid (measured:
+    // 2048^3 0.341 -> 0.324 ms and 8192 x 64 x 8192 0.191 -> 0.169 at 54 per CTA;
+    // 1024^3 at 7 and 1000 x 1300 x 1500 at 14 per CTA were slower than the K
+    // split).
+    if (PG_FFMA_SK && !tc && (bn == 64 || bn == 128) && fs == 0 && allow_tail && tiles < capacity &&
+        100 * tiles * split < PG_FFMA_SK_FILL * capacity && tiles * pl->k_blocks >= PG_FFMA_SK_MIN_KB * capacity &&
+        sk_segs_per_cta(tiles, pl->k_blocks, capacity) <= kSkMaxSegsPerCta) {
+        split = 1;
+        per = pl->k_blocks;
+        pl->sk_ctas = static_cast<int>(capacity);
+    }
     pl->split_k = static_cast<int>(split);
     pl->k_blocks_per_split = static_cast<int>(per);
 
@@ -259,7 +309,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // last wave at most half full, cut each last-wave tile's K into s slices (at
     // least 8 K blocks each, s <= 4) so the last wave keeps every pair (every
     // FFMA CTA slot) busy.
-    if ((pair || !tc) && split == 1 && g_force_split.load() == 0 && allow_tail) {
+    if ((pair || !tc) && split == 1 && pl->sk_ctas == 0 && g_force_split.load() == 0 && allow_tail) {
         const int64_t waves = tiles / capacity, rem = tiles % capacity;
         if (waves >= 1 && rem > 0 && 2 * rem <= capacity) {
             const int64_t s = std::min<int64_t>({capacity / rem, 4, pl->k_blocks / 8});
@@ -276,8 +326,10 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     if (pl->prep_b != SGEMM_PREP_NONE) ws += parts_b * region(pl->ld_b * (rows_b == k ? n : k));
     if (split > 1) ws += region(split * round_up(m, 4) * n);
     if (pl->tail_split > 1) ws += tail_bytes(*pl) + tail_counter_bytes(*pl);
+    if (pl->sk_ctas > 0) ws += region(tiles * sk_maxseg(tiles, pl->k_blocks, pl->sk_ctas) * pl->bm * pl->bn);
     pl->workspace_bytes = ws;
-    pl->launches = (pl->prep_a != SGEMM_PREP_NONE) + (pl->prep_b != SGEMM_PREP_NONE) + 1 + (split > 1);
+    pl->launches = (pl->prep_a != SGEMM_PREP_NONE) + (pl->prep_b != SGEMM_PREP_NONE) + 1 + (split > 1) +
+                   (pl->sk_ctas > 0);
 }
 
 // ---- devices ------------------------------------------------------------------------
@@ -480,7 +532,12 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
                         static_cast<unsigned>(pl.split_k));
         if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
         if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
-        if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) return fail_cuda(e, "FFMA GEMM kernel");
+        if (pl.sk_ctas > 0) {
+            if ((e = launch_ffma_sk(tmA, tmB, gp, pl.bn, pl.sk_ctas, num_sms, st)) != cudaSuccess)
+                return fail_cuda(e, "FFMA stream-K kernels");
+        } else if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) {
+            return fail_cuda(e, "FFMA GEMM kernel");
+        }
     } else {
         // tcgen05: A in 32-row boxes (M-major, 32-byte-atom swizzle), B in boxes of
         // pl.bk x (bn, or bn/2 per CTA on SM pairs).
@@ -663,6 +720,13 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
         gp.tail_cnt = reinterpret_cast<int*>(cursor);
         if ((e = cudaMemsetAsync(gp.tail_cnt, 0, tail_counter_bytes(pl), st)) != cudaSuccess)
             return fail_cuda(e, "cudaMemsetAsync (last-wave counters)");
+    }
+    if (pl.sk_ctas > 0) {
+        const int64_t tiles = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n;
+        gp.sk_iters = tiles * pl.k_blocks;
+        gp.sk_maxseg = sk_maxseg(tiles, pl.k_blocks, pl.sk_ctas);
+        gp.sk_P = reinterpret_cast<float*>(cursor);
+        cursor += region(tiles * gp.sk_maxseg * pl.bm * pl.bn);
     }
     gp.group_m = PG_GROUP_M;
     gp.c_vec = aligned16(C) && (ldc % 4 == 0);

@@ -81,6 +81,13 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
         assert tiles >= capacity, where
     else:
         assert p["tail_split"] == 1, where
+    # FFMA stream-K: only where the tiles (with their K slices) leave over a tenth of
+    # one wave's CTA slots idle and every slot gets at least 32 k-blocks; all slots run
+    if p["sk_ctas"] > 0:
+        tiles = p["tiles_m"] * p["tiles_n"]
+        capacity = sms * p["ctas_per_sm"]
+        assert name == "ffma" and p["bn"] in (64, 128) and s == 1 and p["tail_split"] == 1, where
+        assert p["sk_ctas"] == capacity and tiles < capacity and tiles * p["k_blocks"] >= 32 * capacity, where
     # launch resources fit one SM
     assert 0 < p["smem_bytes"] <= SMEM_PER_CTA, where
     assert p["ctas_per_sm"] * p["smem_bytes"] <= SMEM_PER_SM, where
@@ -110,9 +117,9 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
             assert prep == want, where
     if mode == "3xtf32" and name == "tc2":
         assert p["prep_a_name"] == "split" and p["prep_b_name"] == "split", where
-    # launches: one per preparation, the GEMM, and the reduction of a K split
+    # launches: one per preparation, the GEMM, and the reduction of a K split or the stream-K fix-up
     preps = (p["prep_a_name"] != "none") + (p["prep_b_name"] != "none")
-    assert p["launches"] == preps + 1 + (s > 1), where
+    assert p["launches"] == preps + 1 + (s > 1) + (p["sk_ctas"] > 0), where
     # workspace holds at least the prepared operands and the partial sums
     ws = 0
     for prep, ld_read, rows, elems in ((p["prep_a_name"], p["ld_a"], rows_a, m * k),
@@ -123,8 +130,10 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
         ws += s * _round_up(m, 4) * n * 4
     if p["tail_split"] > 1:
         ws += p["tail_tiles"] * p["tail_split"] * p["bm"] * p["bn"] * 4
+    if p["sk_ctas"] > 0:  # at least one partial block per tile
+        ws += p["tiles_m"] * p["tiles_n"] * p["bm"] * p["bn"] * 4
     assert p["workspace_bytes"] >= ws, where
-    if preps == 0 and s == 1 and p["tail_split"] == 1:
+    if preps == 0 and s == 1 and p["tail_split"] == 1 and p["sk_ctas"] == 0:
         assert p["workspace_bytes"] == 0, where
 
 
