@@ -284,6 +284,40 @@ def run_ours(args, wl_name):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                "api": "sgemm_host_async, one stream per mode (pinned host buffers)"}
 
+    # The hybrid CPU + GPU column split, end to end through the synchronous host
+    # entry: per mode, calls with the automatic ratio (warm-up calls let it settle
+    # on the measured speed ratio) against the same calls with the split off.
+    hybrid = None
+    if args.host_split and world == 1 and not args.skip_e2e:
+        hA, hB = A.pin_memory(), B.pin_memory()
+        hC = C.clone().pin_memory()
+
+        def host_calls(reps):
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                if p.layout == "col":
+                    pg.sgemm_host(p.transa, p.transb, p.m, p.n, p.k, p.alpha, hA, p.lda, hB, p.ldb, p.beta, hC,
+                                  p.ldc, mode, stream)
+                else:
+                    pg.sgemm_host("N", "N", p.n, p.m, p.k, p.alpha, hB, p.ldb, hA, p.lda, p.beta, hC, p.ldc, mode,
+                                  stream)
+            return (time.perf_counter() - t0) / reps
+        hybrid = {"api": "sgemm_host (synchronous, pinned host buffers), one call per mode; host time per call",
+                  "modes": {}}
+        for mode in modes:
+            pg.set_host_split(0.0)
+            host_calls(1)
+            t_off = host_calls(3)
+            pg.set_host_split(-1.0)
+            host_calls(4)  # the automatic ratio settles on the measured speeds
+            t_on = host_calls(3)
+            q = pg.host_split_ratio(mode)
+            pg.set_host_split(0.0)
+            n_cpu = int(p.n // (q + 1.0)) if p.layout == "col" else int(p.m // (q + 1.0))
+            hybrid["modes"][mode] = {"q": q, "cpu_columns": n_cpu, "ms_split_off": t_off * 1e3,
+                                     "ms_split_auto": t_on * 1e3, "tflops_split_off": flops / t_off / 1e12,
+                                     "tflops_split_auto": flops / t_on / 1e12}
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -348,6 +382,8 @@ def run_ours(args, wl_name):
     }
     if sweep is not None:
         line["workloads"] = sweep
+    if hybrid is not None:
+        line["e2e_host_split"] = hybrid
     if not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds, args.cpu_threads)
     if dist:
@@ -518,6 +554,8 @@ def main():
     ap.add_argument("--cpu-threads", type=int, default=0)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--host-split", type=int, default=1,
+                    help="1: also time the hybrid CPU + GPU column split of sgemm_host end to end (0: skip)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-workload timings of the other acceptance configs")
     ap.add_argument("--sweep-reps", type=int, default=5, help="timed calls per mode and workload in the sweep")

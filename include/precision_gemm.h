@@ -162,6 +162,42 @@ int sgemm_host_async(char transa, char transb, int64_t m, int64_t n, int64_t k, 
                      float *C, int64_t ldc, int mode, void *stream);
 
 /*
+ * sgemm_set_host_split -- the hybrid CPU + GPU column split of the host-array
+ * calls ("HPC - Lecture 13 - MatMat GPU", sections "Load distribution" and "the
+ * hybrid function matmatgpu3": the columns of C are divided between the two
+ * devices in proportion to their measured speeds, the GPU kernel runs
+ * asynchronously while the host cores compute their share, then both are
+ * waited for).
+ *
+ *   q  > 0  fixed ratio Q: sgemm_host and sgemm_host_async give the last
+ *           floor(n / (Q + 1)) columns of C to the library's host co-worker (a
+ *           blocked FP32 product on the host cores, OpenMP; every output one
+ *           fused multiply-add chain in increasing p, so deterministic) and the
+ *           rest to the GPU path;
+ *      < 0  automatic: Q per mode starts at the lecture's 15 and every
+ *           synchronous sgemm_host call re-measures it as the ratio of the two
+ *           parts' speeds (columns per second);
+ *      = 0  off (the default): everything on the GPU.
+ *   (1)
+ *
+ * The split applies to calls with a product (k > 0, alpha != 0) and n >= 2;
+ * the host part runs in the calling thread during the call (sgemm_host_async
+ * therefore returns with the host columns of C already written and the GPU
+ * columns queued).  The host columns of B and C never cross the host link.
+ * The host part computes in FP32 in every mode, within every mode's accuracy.
+ * sgemm (device pointers) is not affected.  Applies to calls made afterwards
+ * from any thread.  Returns 0, or -1 when q is not finite.
+ */
+int sgemm_set_host_split(double q);
+
+/*
+ * sgemm_host_split_ratio -- the Q the next host call in `mode` would use: the
+ * fixed ratio, the automatic one as last measured, or 0 when the split is off;
+ * -1 for an invalid mode.
+ */
+double sgemm_host_split_ratio(int mode);
+
+/*
  * sgemm_noalloc -- sgemm without any device allocation.  (The pages have no
  * counterpart: this entry exists for callers of this library, not for the
  * method.)

@@ -44,8 +44,8 @@ KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc", 4: "tc2"}
 PREPS = {0: "none", 1: "copy", 2: "transpose", 3: "split"}
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTS = ("sgemm", "sgemm_host", "sgemm_host_async", "sgemm_noalloc", "sgemm_set_workspace", "sgemm_plan",
-           "sgemm_device_status",
+EXPORTS = ("sgemm", "sgemm_host", "sgemm_host_async", "sgemm_set_host_split", "sgemm_host_split_ratio",
+           "sgemm_noalloc", "sgemm_set_workspace", "sgemm_plan", "sgemm_device_status",
            "sgemm_set_wait_timeout", "sgemm_force_plan", "sgemm_debug_flags", "sgemm_launch_count",
            "sgemm_workspace_release", "sgemm_last_error_string", "sgemm_version")
 
@@ -93,6 +93,10 @@ def load_library(path: str | None = None):
         lib.sgemm_host_async.restype = i
         lib.sgemm_noalloc.argtypes = gemm_args
         lib.sgemm_noalloc.restype = i
+        lib.sgemm_set_host_split.argtypes = [ctypes.c_double]
+        lib.sgemm_set_host_split.restype = i
+        lib.sgemm_host_split_ratio.argtypes = [i]
+        lib.sgemm_host_split_ratio.restype = ctypes.c_double
         lib.sgemm_set_workspace.argtypes = [vp, ctypes.c_size_t, vp]
         lib.sgemm_set_workspace.restype = i
         lib.sgemm_plan.argtypes = gemm_args[:14] + [i, ctypes.POINTER(sgemm_plan_t)]
@@ -263,6 +267,19 @@ def sgemm_rm(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode="ffma", stream=N
     column-major storage of the transpose, so this is the column-major call
     C^T = B^T * A^T: operands swapped, m and n swapped."""
     sgemm("N", "N", n, m, k, alpha, B, ldb, A, lda, beta, C, ldc, mode, stream)
+
+
+def set_host_split(q: float) -> None:
+    """Hybrid CPU + GPU column split of sgemm_host / sgemm_host_async: q > 0 gives
+    the last floor(n / (q + 1)) columns of C to the host cores, q < 0 measures q
+    call by call (starting at 15), 0 turns the split off (the default)."""
+    lib = load_library()
+    _check(lib.sgemm_set_host_split(float(q)), lib)
+
+
+def host_split_ratio(mode="ffma") -> float:
+    """The ratio Q the next host call in `mode` would use (0 when the split is off)."""
+    return float(load_library().sgemm_host_split_ratio(_mode(mode)))
 
 
 _ws_refs = {}  # (device, stream handle) -> the tensor given to set_workspace, kept alive here

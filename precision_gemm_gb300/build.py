@@ -16,9 +16,17 @@ LIB = os.path.join(HERE, "libprecision_gemm.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["sgemm_api.cu", "ffma_kernel.cu", "tc_kernel.cu", "tc2_kernel.cu", "aux_kernels.cu"]
+# Host-only C++ (the CPU co-worker of the hybrid column split), compiled by the host compiler.
+HOST_SOURCES = ["host_sgemm.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]
+# gnu++17 with explicit FMA contraction; no -march: the same flags build on x86 and Arm.
+HOST_FLAGS = ["-O3", "-std=gnu++17", "-fPIC", "-fopenmp", "-ffp-contract=fast", "-fvisibility=hidden"]
+
+
+def _cxx() -> str:
+    return os.environ.get("CXX", "g++")
 
 
 def _nvcc() -> str:
@@ -54,6 +62,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
+    for src in HOST_SOURCES:
+        obj = os.path.join(BUILD, src.replace(".cpp", ".o"))
+        objs.append(obj)
+        cmd = [_cxx(), *HOST_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     failed = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -64,7 +77,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
     tmp = LIB + ".tmp%d" % os.getpid()
-    link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static",
+    link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lgomp",
             "-Xlinker", "-Bsymbolic", "-Xlinker", "--exclude-libs,ALL"]
     subprocess.run(link, check=True)
     os.replace(tmp, LIB)

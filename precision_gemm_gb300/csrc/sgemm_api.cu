@@ -13,6 +13,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -24,6 +26,7 @@
 #include <vector>
 
 #include "../../include/precision_gemm.h"
+#include "host_sgemm.h"
 #include "internal.h"
 
 #define PG_EXPORT extern "C" __attribute__((visibility("default")))
@@ -904,10 +907,10 @@ namespace {
 // all of it.  Without `wait`, `stream` is left ordered after the last copy out,
 // so synchronising it -- or the next call on it, whose copies reuse the staging
 // buffers -- waits for every copy of this call.
-int host_call(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
-              const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode, void* stream, bool wait) {
-    int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
-    if (rc) return rc;
+int host_call_gpu(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
+                  int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,
+                  void* stream, bool wait) {
+    int rc = 0;
     if (m == 0 || n == 0) return 0;
     int dev;
     DeviceState* ds;
@@ -1030,8 +1033,95 @@ int host_call(char transa, char transb, int64_t m, int64_t n, int64_t k, float a
     return rc;
 }
 
+// ---- the hybrid CPU + GPU column split ("HPC - Lecture 13 - MatMat GPU", sections
+// "Load distribution" and "the hybrid function matmatgpu3") ----------------------
+//
+// With a ratio Q set (sgemm_set_host_split), a host call gives the first
+// n - floor(n / (Q + 1)) columns of C to the GPU path above and the last
+// floor(n / (Q + 1)) to the host co-worker (host_sgemm), which runs in the
+// calling thread while the GPU's copies and kernels proceed: the lecture's
+// asynchronous kernel launch followed by matmatthreadomp, then the wait.  The
+// host columns of B and C never cross the host link.  Q < 0 selects the
+// automatic ratio: every synchronous call measures its two parts (the GPU part
+// by events around its queued work, the host part by the host clock) and sets
+// the next Q of its mode to the ratio of their speeds, GFLOP/s of the GPU part
+// over GFLOP/s of the host part -- the lecture's rule of splitting in
+// proportion to the measured performance ratio, re-measured call by call.  It
+// starts from the lecture's Q = 15.
+
+std::atomic<double> g_split_q{0.0};                 // 0: off, > 0: fixed Q, < 0: automatic
+std::atomic<double> g_split_auto[3] = {{15.0}, {15.0}, {15.0}};  // automatic Q per mode
+
+double split_ratio(int mode) {
+    const double q = g_split_q.load();
+    if (q == 0.0) return 0.0;
+    return q > 0.0 ? q : g_split_auto[mode].load();
+}
+
+int host_call(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
+              const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode, void* stream, bool wait) {
+    int rc = validate(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode);
+    if (rc) return rc;
+    const double q = split_ratio(mode);
+    const bool product = m > 0 && n > 1 && k > 0 && alpha != 0.0f;
+    const int64_t n_cpu = (q > 0.0 && product) ? static_cast<int64_t>(std::floor(n / (q + 1.0))) : 0;
+    if (n_cpu <= 0 || n_cpu >= n)
+        return host_call_gpu(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, mode, stream, wait);
+    const int64_t n_gpu = n - n_cpu;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool measure = wait && g_split_q.load() < 0.0;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e;
+    if (measure) {
+        if ((e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess ||
+            (e = cudaEventRecord(e0, st)) != cudaSuccess) {
+            if (e0) cudaEventDestroy(e0);
+            if (e1) cudaEventDestroy(e1);
+            return fail_cuda(e, "events of the host split");
+        }
+    }
+    // the GPU's columns: queued, not waited for
+    rc = host_call_gpu(transa, transb, m, n_gpu, k, alpha, A, lda, B, ldb, beta, C, ldc, mode, stream, false);
+    if (rc == 0 && measure && (e = cudaEventRecord(e1, st)) != cudaSuccess) rc = fail_cuda(e, "cudaEventRecord");
+    // the host's columns, meanwhile (B's columns n_gpu.. are B + n_gpu*ldb when B is
+    // stored k x n, its rows n_gpu.. when stored n x k)
+    double cpu_s = 0.0;
+    if (rc == 0) {
+        const float* Bc = is_notrans(transb) ? B + n_gpu * ldb : B + n_gpu;
+        const auto t0 = std::chrono::steady_clock::now();
+        host_sgemm(transa, transb, m, n_cpu, k, alpha, A, lda, Bc, ldb, beta, C + n_gpu * ldc, ldc, 0);
+        cpu_s = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    }
+    // the GPU's copies touch the caller's arrays: also after a failure, wait for
+    // what was queued before returning an error
+    if ((wait || rc != 0) && (e = cudaStreamSynchronize(st)) != cudaSuccess && rc == 0)
+        rc = fail_cuda(e, "cudaStreamSynchronize");
+    if (rc == 0 && measure) {
+        float gpu_ms = 0.0f;
+        if (cudaEventElapsedTime(&gpu_ms, e0, e1) == cudaSuccess && gpu_ms > 0.0f && cpu_s > 0.0) {
+            const double r_gpu = static_cast<double>(n_gpu) / (1e-3 * gpu_ms);  // columns per second
+            const double r_cpu = static_cast<double>(n_cpu) / cpu_s;
+            g_split_auto[mode] = std::min(1e6, std::max(1.0, r_gpu / r_cpu));
+        }
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    return rc;
+}
+
 }  // namespace
 }  // namespace pg
+
+PG_EXPORT int sgemm_set_host_split(double q) {
+    if (std::isnan(q) || std::isinf(q)) return fail(-1, "argument 1 (q): %g is not a finite ratio", q);
+    g_split_q = q;
+    return 0;
+}
+
+PG_EXPORT double sgemm_host_split_ratio(int mode) {
+    if (mode != SGEMM_FFMA && mode != SGEMM_TF32 && mode != SGEMM_3XTF32) return -1.0;
+    return split_ratio(mode);
+}
 
 PG_EXPORT int sgemm_host(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const float* A,
                          int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc, int mode,

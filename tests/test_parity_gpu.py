@@ -522,6 +522,40 @@ def test_host_buffers_pipelined_slabs(mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("q,tb,mnk", [(3.0, "N", (700, 530, 900)), (1.5, "T", (300, 97, 2000)),
+                                      (-1.0, "N", (700, 530, 900)), (7.0, "N", (2304, 6000, 300))])
+def test_host_split(mode, q, tb, mnk):
+    """The hybrid CPU + GPU column split of the host entry: the last
+    floor(n / (q + 1)) columns of C on the host co-worker, the rest on the GPU
+    path (with n >= 4096 its pipelined column slabs), concurrently; a fixed
+    ratio, and the automatic one re-measured by the call.  The whole C matches
+    the oracle, its ld gaps stay untouched; the asynchronous entry gives the same
+    result after a stream synchronisation."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, transb=tb, ldc=m + 5, alpha=1.25, beta=0.5, dist="normal", seed=103)
+    p = p.with_(lda=p.lda + 3)
+    A, B, C = synth.make(p)
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    Ch, Ca = C.clone().pin_memory(), C.clone().pin_memory()
+    try:
+        pg.set_host_split(q)
+        before = pg.host_split_ratio(mode)
+        pg.sgemm_host(p.transa, p.transb, m, n, k, p.alpha, Ah, p.lda, Bh, p.ldb, p.beta, Ch, p.ldc, mode)
+        if q < 0:
+            assert pg.host_split_ratio(mode) != before  # re-measured from this call's two parts
+        s = torch.cuda.Stream()
+        pg.sgemm_host_async(p.transa, p.transb, m, n, k, p.alpha, Ah, p.lda, Bh, p.ldb, p.beta, Ca, p.ldc, mode, s)
+        s.synchronize()
+    finally:
+        pg.set_host_split(0.0)
+    cref, den = H.reference_full(p, A, B, C)
+    for out in (Ch, Ca):
+        res = oracle.check(H.logical(p, out), cref, den, oracle.TOL[mode])
+        assert res["ok"], res
+        assert H.padding_intact(p, out, C)
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_launch_counter_counts_kernels(mode):
     for p in (synth.Problem(256, 256, 256), synth.Problem(4096, 4096, 512)):
         A, B, C = synth.make(p)
