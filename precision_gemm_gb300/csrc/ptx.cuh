@@ -91,6 +91,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// A warp's wait for a phase of `bar`: lane 0 alone polls (bounded); once it has
+// seen the phase complete, every lane runs its own wait, which then succeeds at
+// its first test and gives that lane the acquire ordering on the data the phase
+// guards (a lane's reads of TMA-written shared memory are ordered only by its
+// own acquire).  One polling lane instead of 32 keeps the barrier's shared-memory
+// traffic off the banks the operand reads use.  Returns the warp-uniform outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                               const volatile int* abort_flag) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, timeout_ns, abort_flag);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, timeout_ns, abort_flag));
+}
+
 // Record a failed wait: raise the CTA's abort flag and the device status word.
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* status) {
     *abort_flag = 1;
