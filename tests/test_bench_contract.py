@@ -125,3 +125,28 @@ def test_profile_summaries_give_runnable_commands():
                 m = re.search(r"--workload (\S+)", c)
                 if m:
                     assert m.group(1) in bench.WORKLOADS, (name, m.group(1))
+
+
+def test_bench_figures_and_config_helpers():
+    """The arithmetic behind the GPU arm's JSON line, without a GPU: per-mode
+    TFLOP/s, the roofline min(compute, AI x HBM) and its bound, the tensor-pipe
+    fraction (3xTF32 counts its three products), and one config for both arms."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from precision_gemm_gb300 import synth
+    pk = {"fp32": 80.0, "tf32": 900.0, "hbm": 6800.0, "pipe": 1289.0}
+    big = synth.Problem(8192, 8192, 8192, beta=1.0)
+    f = bench.mode_figures("ffma", big, 17.2, pk)
+    assert abs(f["tflops"] - 2 * 8192 ** 3 / 17.2e-3 / 1e12) < 1e-9
+    assert f["bound"] == "compute" and f["roofline_tflops"] == 80.0 and "frac_of_tensor_pipe" not in f
+    t = bench.mode_figures("3xtf32", big, 3.0, pk)
+    assert t["compute_peak_tflops"] == 300.0 and abs(t["frac_of_tensor_pipe"] - 3 * t["tflops"] / 1289.0) < 1e-12
+    skinny = synth.Problem(16384, 16384, 64, beta=0.0)
+    s = bench.mode_figures("tf32", skinny, 0.2, pk)
+    ai = 2 * 16384 * 16384 * 64 / bench.alg_bytes(skinny)
+    assert s["bound"] == "hbm" and abs(s["roofline_tflops"] - ai * 6800.0 / 1e3) < 1e-9
+    assert bench.alg_bytes(skinny) == 4 * (16384 * 64 * 2 + 16384 * 16384)
+    cfg = bench.make_config("square8192", bench.WORKLOADS["square8192"][1], ["ffma"], 1)
+    assert cfg["l2"].startswith("inputs larger than L2") and cfg["parallelism"] == "single GPU"
+    assert bench.make_config("square8192", bench.WORKLOADS["square8192"][1], ["ffma"], 4)["parallelism"] == "replicas"
+    assert set(bench.SWEEP) <= set(synth.config_problems())
