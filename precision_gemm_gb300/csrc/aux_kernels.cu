@@ -311,6 +311,76 @@ __global__ void __launch_bounds__(256) splitk_reduce_grouped_kernel(const GemmPa
     }
 }
 
+// Stream-K fix-up (the FFMA and the single-SM tensor-core stream-K kernels):
+// C = alpha * sum_j P[t][j] + beta * C per 128 x BN tile t, the segments j of t
+// added in increasing order -- increasing k, so deterministic.  A thread takes 4 consecutive rows of one column of a tile
+// (one float4 of each partial block), all of its segments' loads issued before
+// the additions; C is read and written as a float4 when it is 16-byte aligned
+// with ldc % 4 == 0 and the 4 rows lie inside C.
+template <int BN>
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmParams p, int G) {
+    constexpr int BM = kBM;
+    constexpr int RQ = BM / 4;       // float4 chunks per tile column
+    constexpr int CH = RQ * BN;      // per tile
+    constexpr int kMaxSeg = 8;       // loads in flight per batch
+    const int64_t T = p.sk_iters;
+    const int kb = p.kb_total;
+    const int64_t total = static_cast<int64_t>(p.tiles_m) * p.tiles_n * CH;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(q / CH);
+        const int r = static_cast<int>(q - static_cast<int64_t>(t) * CH);
+        const int col = r / RQ, row4 = (r - col * RQ) * 4;
+        int tmi, tni;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tmi, tni);
+        const int64_t i = static_cast<int64_t>(tmi) * BM + row4;
+        const int64_t jc = static_cast<int64_t>(tni) * BN + col;
+        if (i >= p.m || jc >= p.n) continue;
+        const int64_t first = static_cast<int64_t>(t) * kb;
+        const int nseg = sk_cta_of(first + kb - 1, G, T) - sk_cta_of(first, G, T) + 1;
+        const float4* src = reinterpret_cast<const float4*>(p.sk_P + static_cast<int64_t>(t) * p.sk_maxseg * (BM * BN) +
+                                                            col * BM + row4);
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int j0 = 0; j0 < nseg; j0 += kMaxSeg) {
+            float4 v[kMaxSeg];
+#pragma unroll
+            for (int u = 0; u < kMaxSeg; ++u)
+                if (j0 + u < nseg) v[u] = __ldcg(src + static_cast<int64_t>(j0 + u) * (BM * BN / 4));
+#pragma unroll
+            for (int u = 0; u < kMaxSeg; ++u) {
+                if (j0 + u < nseg) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
+            }
+        }
+        float* dst = p.C + jc * p.ldc + i;
+        const bool vec = p.c_vec && i + 3 < p.m;
+        float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+        if (p.beta != 0.0f) {
+            float cin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (vec) {
+                const float4 cv = *reinterpret_cast<const float4*>(dst);
+                cin[0] = cv.x;
+                cin[1] = cv.y;
+                cin[2] = cv.z;
+                cin[3] = cv.w;
+            } else {
+                for (int e = 0; e < 4 && i + e < p.m; ++e) cin[e] = dst[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = fmaf(p.beta, cin[e], o[e]);
+        }
+        if (vec) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            for (int e = 0; e < 4 && i + e < p.m; ++e) dst[e] = o[e];
+        }
+    }
+}
+
 // C = beta * C (beta = 0 writes zeros without reading C).
 __global__ void __launch_bounds__(256, 4) scale_kernel(float* __restrict__ C, int64_t ldc, int64_t m, int64_t n,
                                                        float beta, int tx_shift, int by_rows) {
@@ -406,6 +476,19 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t 
     const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
     if (g > cap) g = cap;
     splitk_reduce_vec_kernel<<<static_cast<unsigned>(g), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_streamk_fixup(const GemmParams& p, int bn, int ctas, int num_sms, cudaStream_t stream) {
+    const int64_t chunks = static_cast<int64_t>(p.tiles_m) * p.tiles_n * (kBM / 4) * bn;
+    int64_t g = (chunks + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+    if (g > cap) g = cap;
+    switch (bn) {
+        case 64: streamk_fixup_kernel<64><<<static_cast<unsigned>(g), 256, 0, stream>>>(p, ctas); break;
+        case 128: streamk_fixup_kernel<128><<<static_cast<unsigned>(g), 256, 0, stream>>>(p, ctas); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

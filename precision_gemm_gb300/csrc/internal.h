@@ -83,6 +83,12 @@ size_t tc_smem_bytes(int bn, bool split3);
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
                       int bn, bool split3, dim3 grid, cudaStream_t stream);
 
+// The same kernel in stream-K form (3xTF32, bn = 128): `ctas` CTAs share
+// the (tile, k-block) iterations in equal ranges, storing partial blocks to
+// p.sk_P; launch_streamk_fixup then sums them.
+cudaError_t launch_tc_sk(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
+                         int bn, int ctas, cudaStream_t stream);
+
 // tcgen05 kernel on SM pairs (cta_group::2, persistent, double-buffered TMEM):
 // pair tile 256 x bn, bn in {128, 256}; launches min(units, resident pairs) pairs.
 int tc2_bk(bool split3);
@@ -104,6 +110,12 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
 
 // C = alpha * sum_s P[s] + beta * C, slices summed in increasing s.
 cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// Stream-K fix-up: C = alpha * sum_j P[t][j] + beta * C per 128 x bn tile t
+// (bn in {64, 128}), the partial blocks p.sk_P + (t * sk_maxseg + j) * 128 * bn
+// ([column][row]) of its segments j added in increasing order; `ctas` is the
+// stream-K grid, whose ranges give each tile's number of segments.
+cudaError_t launch_streamk_fixup(const GemmParams& p, int bn, int ctas, int num_sms, cudaStream_t stream);
 
 // C = beta * C (beta == 0 writes zeros without reading C).
 cudaError_t launch_scale(float* C, int64_t ldc, int64_t m, int64_t n, float beta, int num_sms,

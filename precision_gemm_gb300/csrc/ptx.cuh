@@ -410,6 +410,12 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
     return v;
 }
 
+// Stream-K: the CTA whose range [c T / G, (c + 1) T / G) of the T (tile,
+// k-block) iterations holds iteration `it` -- the largest c with c T / G <= it.
+__device__ __forceinline__ int sk_cta_of(int64_t it, int G, int64_t T) {
+    return static_cast<int>(((it + 1) * G - 1) / T);
+}
+
 // Output tile position for CTA `tile` under grouped rasterisation: consecutive
 // CTAs walk `group_m` tile rows of one tile column before moving right, so a
 // wave of CTAs shares A row-panels and B column-panels in L2.

@@ -56,7 +56,15 @@ namespace {
 #ifndef PG_FFMA_SK_MIN_KB
 #define PG_FFMA_SK_MIN_KB 32  // k-blocks per CTA at least
 #endif
-constexpr int kSkMaxSegsPerCta = 8;  // the kernel's segment table
+constexpr int kSkMaxSegsPerCta = 8;  // the kernels' segment tables
+// 3xTF32 stream-K on the single-SM tensor-core kernel (a compile-time switch),
+// at least PG_TC_SK_MIN_KB k-blocks per CTA.
+#ifndef PG_TC_SK
+#define PG_TC_SK 1
+#endif
+#ifndef PG_TC_SK_MIN_KB
+#define PG_TC_SK_MIN_KB 32
+#endif
 
 
 constexpr int kMaxDevices = 64;
@@ -300,6 +308,19 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // split).
     if (PG_FFMA_SK && !tc && (bn == 64 || bn == 128) && fs == 0 && allow_tail && tiles < capacity &&
         100 * tiles * split < PG_FFMA_SK_FILL * capacity && tiles * pl->k_blocks >= PG_FFMA_SK_MIN_KB * capacity &&
+        sk_segs_per_cta(tiles, pl->k_blocks, capacity) <= kSkMaxSegsPerCta) {
+        split = 1;
+        per = pl->k_blocks;
+        pl->sk_ctas = static_cast<int>(capacity);
+    }
+    // 3xTF32 stream-K on the single-SM kernel's 128-wide tiles whose products
+    // fill less than 90 % of the SMs even with a K split: every SM is given an
+    // equal share.  Measured (L2 flushed): 8192 x 128 x 8192 0.102 -> 0.097 ms,
+    // 4096 x 128 x 8192 0.064 -> 0.062, 128 x 4096 x 8192 0.067 -> 0.063; on the
+    // 64-wide tile slower (8192 x 64 x 8192 0.083 -> 0.089, 5000 x 60 x 12000
+    // 0.082 -> 0.084), so it keeps the K split there.
+    if (PG_TC_SK && split3 && !pair && bn == 128 && fs == 0 && allow_tail && tiles < capacity &&
+        100 * tiles * split < PG_FFMA_SK_FILL * capacity && tiles * pl->k_blocks >= PG_TC_SK_MIN_KB * capacity &&
         sk_segs_per_cta(tiles, pl->k_blocks, capacity) <= kSkMaxSegsPerCta) {
         split = 1;
         per = pl->k_blocks;
@@ -589,9 +610,16 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
             CUtensorMap tmBs = tmB;
             gp.b_presplit = (split3 && b_small != nullptr) ? 1 : 0;
             if (gp.b_presplit && (rc = encode_b(&tmBs, b_small))) return rc;
-            const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
-            if ((e = launch_tc(tmA, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
-                return fail_cuda(e, "tcgen05 GEMM kernel");
+            if (pl.sk_ctas > 0) {
+                if ((e = launch_tc_sk(tmA, tmB, tmBs, gp, pl.bn, pl.sk_ctas, st)) != cudaSuccess)
+                    return fail_cuda(e, "tcgen05 stream-K GEMM kernel");
+                if ((e = launch_streamk_fixup(gp, pl.bn, pl.sk_ctas, num_sms, st)) != cudaSuccess)
+                    return fail_cuda(e, "stream-K fix-up");
+            } else {
+                const dim3 grid(static_cast<unsigned>(pl.tiles_m * pl.tiles_n), static_cast<unsigned>(pl.split_k));
+                if ((e = launch_tc(tmA, tmB, tmBs, gp, pl.bn, split3, grid, st)) != cudaSuccess)
+                    return fail_cuda(e, "tcgen05 GEMM kernel");
+            }
         }
     }
     if (pl.split_k > 1) {

@@ -147,11 +147,23 @@ struct TcCfg {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
 };
 
-template <int BN, bool SPLIT3>
+// At most this many tile segments per stream-K CTA (the planner keeps to it).
+constexpr int kTcSkMaxSegs = 8;
+
+// SK (3xTF32 with BN <= 128; launched for BN = 128): stream-K.  The grid's CTAs share the T =
+// tiles x k-blocks (tile, k-block) iterations in equal contiguous ranges
+// [c T / G, (c + 1) T / G), crossing tile boundaries; the accumulator is drained
+// into a partial block at the end of each tile segment (slot t * sk_maxseg + j
+// for the j-th CTA touching tile t) and restarted for the next, and a fix-up
+// kernel adds each tile's blocks in k order.  The MMA thread waits for the
+// epilogue warps to have drained the accumulator (acc_empty) before the next
+// segment's first MMA.
+template <int BN, bool SPLIT3, bool SK>
 __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBs, const GemmParams p) {
     using Cfg = TcCfg<BN, SPLIT3>;
+    static_assert(!SK || (SPLIT3 && Cfg::FUSED && Cfg::KPS == 1), "stream-K: fused 3xTF32, one k-block per slot");
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
@@ -170,15 +182,24 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    int tile_m, tile_n;
-    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
+    // Stream-K: this CTA's tile segments (partial-block slot, k-blocks, first
+    // k-block, tile origin), built by thread 0; the barriers of the accumulator's
+    // hand-back (acc_empty) and of the last MMA (done).
+    __shared__ int seg_slot[SK ? kTcSkMaxSegs : 1], seg_len[SK ? kTcSkMaxSegs : 1], seg_k0[SK ? kTcSkMaxSegs : 1],
+        seg_m0[SK ? kTcSkMaxSegs : 1], seg_n0[SK ? kTcSkMaxSegs : 1];
+    __shared__ int sk_nsegs, sk_nits;
+    __shared__ __align__(8) uint64_t sk_bars[2];
+    const uint32_t acc_empty_bar = smem_u32(&sk_bars[0]);
+    const uint32_t done_bar = smem_u32(&sk_bars[1]);
+
+    int tile_m = 0, tile_n = 0;
+    if (!SK) tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
     const int64_t m0 = static_cast<int64_t>(tile_m) * Cfg::BM;
     const int64_t n0 = static_cast<int64_t>(tile_n) * BN;
-    const int slice = blockIdx.y;
+    const int slice = SK ? 0 : blockIdx.y;
     const int kb0 = slice * p.kb_per_split;
     const int nkb = min(kb0 + p.kb_per_split, p.kb_total) - kb0;
     constexpr int KPS = Cfg::KPS;
-    const int nst = (nkb + KPS - 1) / KPS;  // ring slots' worth of k-blocks; the last may hold fewer
     // B arrives split (big through tmB, remainders through tmBs into the space in
     // front of B): the transform warps split A only.
     const bool b_presplit = Cfg::FUSED && p.b_presplit != 0;
@@ -192,6 +213,38 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
         for (int j = 0; j < SS; ++j) mbar_init(small_empty0 + 8 * j, 1);
         mbar_init(accum_bar, 1);
         *abort_flag = 0;
+        if (SK) {
+            mbar_init(acc_empty_bar, 4);  // the four epilogue warps
+            mbar_init(done_bar, 1);
+            const int G = gridDim.x, c = blockIdx.x;
+            const int64_t T = p.sk_iters;
+            const int kb = p.kb_total;
+            const int64_t it0 = static_cast<int64_t>(c) * T / G, it1 = static_cast<int64_t>(c + 1) * T / G;
+            int ns = 0;
+            int64_t covered = 0;
+            for (int64_t it = it0; it < it1 && ns < kTcSkMaxSegs; ++ns) {
+                const int tile = static_cast<int>(it / kb);
+                const int k0 = static_cast<int>(it - static_cast<int64_t>(tile) * kb);
+                const int len = static_cast<int>(min(static_cast<int64_t>(kb - k0), it1 - it));
+                int tm_, tn_;
+                tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm_, tn_);
+                seg_slot[SK ? ns : 0] = tile * p.sk_maxseg + (c - sk_cta_of(static_cast<int64_t>(tile) * kb, G, T));
+                seg_len[SK ? ns : 0] = len;
+                seg_k0[SK ? ns : 0] = k0;
+                seg_m0[SK ? ns : 0] = tm_ * Cfg::BM;
+                seg_n0[SK ? ns : 0] = tn_ * BN;
+                it += len;
+                covered += len;
+            }
+            sk_nsegs = ns;
+            sk_nits = static_cast<int>(it1 - it0);
+            // the planner keeps every CTA within kTcSkMaxSegs segments; were the
+            // range longer, report a failure rather than leave part of it undone
+            if (covered != it1 - it0) {
+                sk_nits = 0;
+                raise_abort(abort_flag, p.status);
+            }
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -202,6 +255,8 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
+    // ring slots' worth of k-blocks; the last may hold fewer
+    const int nst = SK ? sk_nits : (nkb + KPS - 1) / KPS;
 
     if (warp == 0) {
         // ---------------- TMA loader ----------------
@@ -210,46 +265,54 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             prefetch_tmap(&tmB);
             if (b_presplit) prefetch_tmap(&tmBs);
             int issued = 0;
+            int ld_seg = 0, ld_kq = 0;  // stream-K: the loader's segment and k-block in it
             if (!(p.debug_flags & 1)) {
                 for (int it = 0; it < nst; ++it) {
                     const int s = it % S;
+                    const int64_t lm0 = SK ? seg_m0[SK ? ld_seg : 0] : m0;
+                    const int64_t ln0 = SK ? seg_n0[SK ? ld_seg : 0] : n0;
+                    const int lkb0 = SK ? seg_k0[SK ? ld_seg : 0] + ld_kq : kb0 + it * KPS;
+                    if (SK && ++ld_kq == seg_len[SK ? ld_seg : 0]) {
+                        ld_kq = 0;
+                        ++ld_seg;
+                    }
                     if (!mbar_wait_bounded(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                         raise_abort(abort_flag, p.status);
                         break;
                     }
                     const uint32_t full = full0 + 8 * s;
-                    const int nsub = min(KPS, nkb - it * KPS);
+                    const int nsub = SK ? 1 : min(KPS, nkb - it * KPS);  // stream-K: one k-block per slot
                     mbar_arrive_expect_tx(full, nsub * (Cfg::LOAD_BYTES + (b_presplit ? Cfg::B_BYTES : 0)));
                     for (int u = 0; u < nsub; ++u) {
-                        const int32_t kc = (kb0 + it * KPS + u) * Cfg::BK;
+                        const int32_t kc = (lkb0 + u) * Cfg::BK;
                         const uint32_t slot = smem_u32(smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES);
                         // A K-major (transa 'T'): one box of 128 rows x BK.  A M-major: one 3-D
                         // box {32 rows, BK, 4 row groups} when m % 32 == 0, else four 2-D boxes
                         // of 32 rows (both land as 4 x [BK][32] row groups).
                         auto load_a = [&](uint32_t dst, const CUtensorMap* map) {
                             if (p.a_kmajor) {
-                                tma_load_2d(dst, map, kc, static_cast<int32_t>(m0), full);
+                                tma_load_2d(dst, map, kc, static_cast<int32_t>(lm0), full);
                             } else if (p.a3d) {
-                                tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(m0 / 32), full);
+                                tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(lm0 / 32), full);
                             } else {
 #pragma unroll
                                 for (int g = 0; g < 4; ++g)
-                                    tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(m0 + 32 * g), kc,
-                                                full);
+                                    tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(lm0 + 32 * g),
+                                                kc, full);
                             }
                         };
                         // B K-major: one box of BN columns x BK.  B N-major (transb 'T'): BN/32
                         // groups of 32 columns, as one 3-D box or as 2-D boxes.
                         auto load_b = [&](uint32_t dst, const CUtensorMap* map) {
                             if (!p.b_mnmajor) {
-                                tma_load_2d(dst, map, kc, static_cast<int32_t>(n0), full);
+                                tma_load_2d(dst, map, kc, static_cast<int32_t>(ln0), full);
                             } else if (p.b3d) {
-                                tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(n0 / 32), full);
+                                tma_load_3d(dst, map, 0, kc, static_cast<int32_t>(ln0 / 32), full);
                             } else {
 #pragma unroll
                                 for (int g = 0; g < BN / 32; ++g)
-                                    tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(n0 + 32 * g), kc,
-                                                full);
+                                    tma_load_2d(dst + g * Cfg::A_BOX_BYTES, map, static_cast<int32_t>(ln0 + 32 * g),
+                                                kc, full);
                             }
                         };
                         load_a(slot, &tmA);
@@ -284,14 +347,24 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
             const uint32_t a_kstep = a_k ? 2 : 64, b_kstep = b_k ? 2 : 64;  // 32 B or 1 KiB per k-step
             int s = 0, j = 0;  // ring slot, remainder slot and TMEM stage (3xTF32)
             uint32_t phase = 0;
+            int seg = 0, seg_left = SK ? seg_len[0] : 0;  // stream-K: the segment and its k-blocks to come
             for (int it = 0; it < nst; ++it) {
                 // 3xTF32: the transform warps have split the slot
                 if (!mbar_wait_bounded((SPLIT3 ? ready0 : full0) + 8 * s, phase, p.timeout_ns, abort_flag)) {
                     raise_abort(abort_flag, p.status);
                     break;
                 }
+                if (SK && seg > 0 && seg_left == seg_len[SK ? seg : 0]) {
+                    // the segment's first k-block: the epilogue warps must have drained
+                    // the previous segment's sums out of the accumulator
+                    if (!mbar_wait_bounded(acc_empty_bar, (seg - 1) & 1, p.timeout_ns, abort_flag)) {
+                        raise_abort(abort_flag, p.status);
+                        break;
+                    }
+                    accumulate = 0;
+                }
                 tc_fence_after_sync();
-                const int nsub = min(KPS, nkb - it * KPS);
+                const int nsub = SK ? 1 : min(KPS, nkb - it * KPS);  // stream-K: one k-block per slot
                 for (int u = 0; u < nsub; ++u) {
                     const uint32_t off = static_cast<uint32_t>(s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES) >> 4;
                     const uint32_t soff =
@@ -325,13 +398,18 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                 }
                 mma_commit(empty0 + 8 * s);  // slot reusable once these MMAs have read it
                 if (SPLIT3) mma_commit(small_empty0 + 8 * j);  // and so is the remainder slot
+                if (SK && --seg_left == 0) {  // the segment's sums are complete
+                    mma_commit(accum_bar);
+                    if (++seg < sk_nsegs) seg_left = seg_len[SK ? seg : 0];
+                }
                 if (++s == S) {
                     s = 0;
                     phase ^= 1;
                 }
                 if (SS > 0 && ++j == SS) j = 0;
             }
-            mma_commit(accum_bar);  // accumulator complete (also after an abort)
+            // the accumulator is complete (also after an abort); stream-K: every MMA has finished
+            mma_commit(SK ? done_bar : accum_bar);
         }
         __syncwarp();
     } else if (warp >= 6) {
@@ -359,7 +437,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     if (lane == 0) raise_abort(abort_flag, p.status);
                     break;
                 }
-                const int nsub = min(KPS, nkb - it * KPS);
+                const int nsub = SK ? 1 : min(KPS, nkb - it * KPS);  // stream-K: one k-block per slot
                 for (int u = 0; u < nsub; ++u) {
                     uint8_t* slot = smem + s * Cfg::STAGE_BYTES + u * Cfg::SUB_BYTES;
                     // A row 32q + lane: its BK values.  K-major: 128-byte row in the
@@ -403,6 +481,37 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ready0 + 8 * s);
             }
+        }
+    } else if (SK) {
+        // ---------------- stream-K epilogue (warps 2..5) ----------------
+        // Per segment: the accumulator (the two halves of the fused form added)
+        // goes to the segment's partial block as [column][row] -- lane = row, so
+        // every store of a warp covers 128 contiguous bytes -- and is handed back.
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        constexpr int EC = 16;
+        for (int seg = 0; seg < sk_nsegs; ++seg) {
+            const bool ready =
+                __all_sync(0xffffffffu, mbar_wait_bounded(accum_bar, seg & 1, p.timeout_ns, abort_flag));
+            if (!ready) {
+                if (lane == 0) raise_abort(abort_flag, p.status);
+                break;
+            }
+            tc_fence_after_sync();
+            float* part = p.sk_P + static_cast<int64_t>(seg_slot[SK ? seg : 0]) * (Cfg::BM * BN) + 32 * q + lane;
+#pragma unroll 1
+            for (int c = 0; c < BN / EC; ++c) {
+                uint32_t v[EC], w[EC];
+                tmem_ld_32x32b_x16(lane_base + EC * c, v);
+                tmem_ld_32x32b_x16(lane_base + BN + EC * c, w);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < EC; ++t)
+                    part[(EC * c + t) * Cfg::BM] = __uint_as_float(v[t]) + __uint_as_float(w[t]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty_bar);
         }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
@@ -473,7 +582,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     if (warp == 1) {
         if (*abort_flag) {
             // MMAs issued before an abort must finish before TMEM is released.
-            if (lane == 0) mbar_wait_bounded(accum_bar, 0, p.timeout_ns, nullptr);
+            if (lane == 0) mbar_wait_bounded(SK ? done_bar : accum_bar, 0, p.timeout_ns, nullptr);
             __syncwarp();
         }
         tc_fence_after_sync();
@@ -481,11 +590,11 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     }
 }
 
-template <int BN, bool SPLIT3>
+template <int BN, bool SPLIT3, bool SK = false>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
                         dim3 grid, cudaStream_t stream) {
     using Cfg = TcCfg<BN, SPLIT3>;
-    auto kern = tc_gemm_kernel<BN, SPLIT3>;
+    auto kern = tc_gemm_kernel<BN, SPLIT3, SK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
@@ -524,6 +633,13 @@ int tc_threads(int bn, bool split3) {
     return bn == 64 ? TcCfg<64, true>::THREADS : (bn == 128 ? TcCfg<128, true>::THREADS : TcCfg<256, true>::THREADS);
 }
 size_t tc_smem_bytes(int bn, bool split3) { return split3 ? smem_of<true>(bn) : smem_of<false>(bn); }
+
+cudaError_t launch_tc_sk(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
+                         int bn, int ctas, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(ctas), 1);
+    if (bn != 128) return cudaErrorInvalidValue;  // the planner takes stream-K for the 128-wide tile only
+    return launch_impl<128, true, true>(tmA, tmB, tmBs, p, grid, stream);
+}
 
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBs, const GemmParams& p,
                       int bn, bool split3, dim3 grid, cudaStream_t stream) {

@@ -138,11 +138,11 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
     t = plan(8192, 64, 8192, "3xtf32")
     assert t["kernel_name"] == "tc" and t["prep_a_name"] == "none" and t["prep_b_name"] == "split"
     assert t["threads"] - plan(8192, 64, 8192, "tf32")["threads"] in (128, 256)
-    assert t["launches"] == 2 + (t["split_k"] > 1)
+    assert t["launches"] == 2 + (t["split_k"] > 1 or t["sk_ctas"] > 0)  # the reduction or the stream-K fix-up
     assert t["workspace_bytes"] >= 2 * 64 * 8192 * 4
     w = plan(128, 4096, 8192, "3xtf32")
     assert w["kernel_name"] == "tc" and w["prep_a_name"] == "none" and w["prep_b_name"] == "none"
-    assert w["launches"] == 1 + (w["split_k"] > 1)
+    assert w["launches"] == 1 + (w["split_k"] > 1 or w["sk_ctas"] > 0)
     assert plan(384, 64, 8192, "3xtf32")["prep_b_name"] == "none"    # three rows of tiles
     assert plan(512, 64, 8192, "3xtf32")["prep_b_name"] == "split"   # four
     assert plan(8192, 64, 8192, "tf32")["prep_b_name"] == "none"     # TF32 reads B as stored

@@ -292,6 +292,36 @@ def test_ffma_stream_k(mnk, ldc_pad, beta):
     assert H.padding_intact(p, out1, C)
 
 
+@pytest.mark.parametrize("mnk,trans,beta", [((8192, 128, 8192), "NN", 0.0), ((4096, 128, 8192), "NN", 1.5),
+                                              ((128, 4096, 8192), "NN", -0.5), ((5100, 100, 9000), "TN", 0.25),
+                                              ((5000, 120, 12000), "NT", 1.0), ((120, 5000, 9000), "TT", 0.0)])
+def test_tc_stream_k(mnk, trans, beta):
+    """3xTF32 on single SMs whose tiles would fill less than 90 % of the SMs runs
+    stream-K: every SM an equal range of (tile, k-block) iterations, the
+    accumulator drained to a partial block at each tile boundary and restarted,
+    a fix-up adding the blocks in k order.  128-wide tiles, B split by the
+    pre-pass or on chip, K- and N-major operands, ragged edges, beta 0 and not:
+    the oracle within 1e-5, bitwise repeatable."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, transa=trans[0], transb=trans[1], alpha=0.75, beta=beta, dist="normal", seed=113)
+    p = p.with_(ldc=p.ldc + 3)
+    plan = pg.sgemm_plan(p.transa, p.transb, m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "3xtf32")
+    assert plan["kernel_name"] == "tc" and plan["sk_ctas"] > 0, plan
+    A, B, C = synth.make(p)
+    out1, ok1 = H.run_gpu(p, "3xtf32", A, B, C)
+    out2, ok2 = H.run_gpu(p, "3xtf32", A, B, C)
+    assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    if m * n <= 2 ** 20:
+        cref, den = H.reference_full(p, A, B, C)
+        res = oracle.check(H.logical(p, out1), cref, den, oracle.TOL["3xtf32"])
+    else:
+        ii, jj = synth.sample_entries(p.m, p.n, count=4096, seed=12345)
+        cref, den = H.reference_entries(p, A, B, C, ii, jj)
+        res = oracle.check(H.gather(p, out1, ii, jj), cref, den, oracle.TOL["3xtf32"])
+    assert res["ok"], res
+    assert H.padding_intact(p, out1, C)
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("mnk", [(1, 1, 1), (1, 300, 7), (300, 1, 7), (5, 3, 1), (127, 129, 33), (131, 67, 255),
                                  (128, 256, 32), (257, 513, 1031), (64, 64, 200000), (160, 200, 300), (288, 130, 77),

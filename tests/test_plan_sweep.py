@@ -83,10 +83,11 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
         assert p["tail_split"] == 1, where
     # FFMA stream-K: only where the tiles (with their K slices) leave over a tenth of
     # one wave's CTA slots idle and every slot gets at least 32 k-blocks; all slots run
-    if p["sk_ctas"] > 0:
+    if p["sk_ctas"] > 0:  # FFMA, or 3xTF32 on single SMs
         tiles = p["tiles_m"] * p["tiles_n"]
         capacity = sms * p["ctas_per_sm"]
-        assert name == "ffma" and p["bn"] in (64, 128) and s == 1 and p["tail_split"] == 1, where
+        assert (name == "ffma" and p["bn"] in (64, 128)) or (name == "tc" and mode == "3xtf32" and p["bn"] == 128), where
+        assert s == 1 and p["tail_split"] == 1, where
         assert p["sk_ctas"] == capacity and tiles < capacity and tiles * p["k_blocks"] >= 32 * capacity, where
     # launch resources fit one SM
     assert 0 < p["smem_bytes"] <= SMEM_PER_CTA, where
