@@ -329,12 +329,24 @@ uint64_t sgemm_set_wait_timeout(uint64_t ns);
 int sgemm_force_plan(int bn, int split_k);
 
 /*
- * sgemm_debug_flags -- test hook.  SGEMM_DEBUG_STALL_PRODUCER makes the
- * operand loader of later GEMM kernels issue nothing, so the waits of the
- * rest of the CTA expire (used by the failure-detection test); 0 clears.
- * Returns the previous flags.
+ * sgemm_debug_flags -- test hooks for failure detection, injected on the
+ * host or as a wait that cannot complete, never as a GPU fault.
+ *   SGEMM_DEBUG_STALL_PRODUCER     the operand loader of later GEMM kernels
+ *                                  issues nothing, so the rest of the CTA's
+ *                                  bounded waits expire (SGEMM_ERR_TIMEOUT in
+ *                                  sgemm_device_status);
+ *   SGEMM_DEBUG_FAIL_ALLOC         a workspace or staging allocation the call
+ *                                  needs fails: the call returns SGEMM_ERR_ALLOC
+ *                                  before any GEMM kernel is launched;
+ *   SGEMM_DEBUG_FAIL_TENSOR_MAP    the TMA tensor-map encoding fails: the call
+ *                                  returns SGEMM_ERR_TENSOR_MAP before the GEMM
+ *                                  kernel is launched (operand preparation may
+ *                                  have run; C is not written).
+ * 0 clears.  Returns the previous flags.
  */
 #define SGEMM_DEBUG_STALL_PRODUCER 1
+#define SGEMM_DEBUG_FAIL_ALLOC 2
+#define SGEMM_DEBUG_FAIL_TENSOR_MAP 4
 int sgemm_debug_flags(int flags);
 
 /* Kernels this library has launched in this process (all devices). */

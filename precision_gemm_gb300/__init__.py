@@ -40,6 +40,10 @@ SGEMM_ERR_SCRATCH = 8
 SGEMM_ERR_WORKSPACE = 9
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_DEBUG_STALL_PRODUCER = 1
+SGEMM_DEBUG_FAIL_ALLOC = 2
+SGEMM_DEBUG_FAIL_TENSOR_MAP = 4
+SGEMM_ERR_ALLOC = 5
+SGEMM_ERR_TENSOR_MAP = 6
 KERNELS = {0: "none", 1: "scale", 2: "ffma", 3: "tc", 4: "tc2"}
 PREPS = {0: "none", 1: "copy", 2: "transpose", 3: "split"}
 

@@ -439,6 +439,8 @@ int get_buffer(int dev, cudaStream_t st, int purpose, size_t need, void** out) {
         return fail(SGEMM_ERR_CAPTURE,
                     "workspace must grow to %zu bytes during stream capture; make one call of this size "
                     "before capturing", need);
+    if (g_debug.load() & SGEMM_DEBUG_FAIL_ALLOC)
+        return fail(SGEMM_ERR_ALLOC, "injected allocation failure (SGEMM_DEBUG_FAIL_ALLOC) for %zu bytes", need);
     if (b.ptr) {
         if ((e = cudaFreeAsync(b.ptr, st)) != cudaSuccess) return fail_cuda(e, "cudaFreeAsync(workspace)");
         b.ptr = nullptr;
@@ -509,6 +511,8 @@ int encode_mn3d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols,
                 uint32_t groups, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled is unavailable from the driver");
+    if (g_debug.load() & SGEMM_DEBUG_FAIL_TENSOR_MAP)
+        return fail(SGEMM_ERR_TENSOR_MAP, "injected tensor-map failure (SGEMM_DEBUG_FAIL_TENSOR_MAP)");
     const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows / 32)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, 32 * 4};
     const cuuint32_t box[3] = {32, box_cols, groups};
@@ -528,6 +532,8 @@ int encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, i
               uint32_t box_cols, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled is unavailable from the driver");
+    if (g_debug.load() & SGEMM_DEBUG_FAIL_TENSOR_MAP)
+        return fail(SGEMM_ERR_TENSOR_MAP, "injected tensor-map failure (SGEMM_DEBUG_FAIL_TENSOR_MAP)");
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
     const cuuint32_t box[2] = {box_rows, box_cols};

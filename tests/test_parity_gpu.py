@@ -647,3 +647,33 @@ def test_bounded_wait_reports_timeout(mode):
     assert pg.device_status(clear=True) == pg.SGEMM_ERR_TIMEOUT
     assert pg.device_status() == 0
     _assert_ok(H.check_problem(p, mode), "after a timeout " + mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_injected_host_faults_fail_cleanly(mode):
+    """Failures injected on the host (an allocation that fails, a tensor map that
+    cannot be encoded) come back as SGEMM_ERR_ALLOC / SGEMM_ERR_TENSOR_MAP from
+    the call itself, leave C untouched and the context usable: the next call on
+    the same stream is correct."""
+    # lda not a multiple of 4: the call needs workspace for an operand copy
+    p = synth.Problem(300, 200, 5000, lda=301, alpha=1.0, beta=0.5, dist="normal", seed=127)
+    A, B, C = synth.make(p)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    s = torch.cuda.Stream()  # a fresh stream: its workspace must be allocated
+    old = pg.debug_flags(0)
+    try:
+        for flag, code in ((pg.SGEMM_DEBUG_FAIL_ALLOC, pg.SGEMM_ERR_ALLOC),
+                           (pg.SGEMM_DEBUG_FAIL_TENSOR_MAP, pg.SGEMM_ERR_TENSOR_MAP)):
+            pg.debug_flags(flag)
+            with pytest.raises(pg.SgemmError) as e:
+                pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+            assert e.value.code == code and "injected" in str(e.value)
+    finally:
+        pg.debug_flags(old)
+    s.synchronize()
+    assert torch.equal(dC.cpu().view(torch.int32), C.view(torch.int32))
+    pg.sgemm("N", "N", p.m, p.n, p.k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    s.synchronize()
+    cref, den = H.reference_full(p, A, B, C)
+    assert oracle.check(H.logical(p, dC.cpu()), cref, den, oracle.TOL[mode])["ok"]
+    assert pg.device_status() == 0
