@@ -147,3 +147,37 @@ def test_captured_last_wave_split_replays(mode):
         torch.cuda.synchronize()
         assert torch.equal(dC.cpu().view(torch.int32), first.view(torch.int32))
     assert pg.device_status() == 0
+
+
+@pytest.mark.parametrize("mode,mnk,trans", [("ffma", (2048, 2048, 2048), "NN"), ("ffma", (1500, 1300, 6000), "TT"),
+                                            ("3xtf32", (4096, 128, 8192), "NN"), ("3xtf32", (120, 5000, 9000), "TN")])
+def test_stream_k_captured_and_replayed(mode, mnk, trans):
+    """Stream-K calls (FFMA, and 3xTF32 on single SMs; with transposed operands the
+    FFMA path copies them first) are plain stream-ordered launches: once the
+    stream's workspace is sized they can be captured into a CUDA graph and
+    replayed on new data, matching the oracle each time."""
+    m, n, k = mnk
+    p = synth.Problem(m, n, k, transa=trans[0], transb=trans[1], alpha=1.25, beta=-0.5, dist="normal", seed=131)
+    plan = pg.sgemm_plan(p.transa, p.transb, m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, mode)
+    assert plan["sk_ctas"] > 0, plan
+    A, B, C = synth.make(p)
+    s = torch.cuda.Stream()
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    with torch.cuda.stream(s):
+        pg.sgemm(p.transa, p.transb, m, n, k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pg.sgemm(p.transa, p.transb, m, n, k, p.alpha, dA, p.lda, dB, p.ldb, p.beta, dC, p.ldc, mode, s)
+    for seed in (132, 133):
+        A2, B2, C2 = synth.make(p.with_(seed=seed))
+        dA.copy_(A2)
+        dB.copy_(B2)
+        dC.copy_(C2)
+        g.replay()
+        torch.cuda.synchronize()
+        ii, jj = synth.sample_entries(p.m, p.n, count=4096, seed=seed)
+        cref, den = H.reference_entries(p, A2, B2, C2, ii, jj)
+        res = oracle.check(H.gather(p, dC.cpu(), ii, jj), cref, den, oracle.TOL[mode])
+        assert res["ok"], (mode, seed, res)
+    assert pg.device_status() == 0
