@@ -150,14 +150,14 @@ struct TcCfg {
 // At most this many tile segments per stream-K CTA (the planner keeps to it).
 constexpr int kTcSkMaxSegs = 8;
 
-// SK (3xTF32 with BN <= 128; launched for BN = 128): stream-K.  The grid's CTAs share the T =
-// tiles x k-blocks (tile, k-block) iterations in equal contiguous ranges
-// [c T / G, (c + 1) T / G), crossing tile boundaries; the accumulator is drained
-// into a partial block at the end of each tile segment (slot t * sk_maxseg + j
-// for the j-th CTA touching tile t) and restarted for the next, and a fix-up
-// kernel adds each tile's blocks in k order.  The MMA thread waits for the
-// epilogue warps to have drained the accumulator (acc_empty) before the next
-// segment's first MMA.
+// SK: stream-K (3xTF32 with BN <= 128; the planner takes it for BN = 128).  The
+// grid's CTAs share the T = tiles x k-blocks (tile, k-block) iterations in equal
+// contiguous ranges [c T / G, (c + 1) T / G), crossing tile boundaries; the
+// accumulator is drained into a partial block at the end of each tile segment
+// (slot t * sk_maxseg + j for the j-th CTA touching tile t) and restarted for the
+// next, and a fix-up kernel adds each tile's blocks in k order.  The MMA thread
+// waits for the epilogue warps to have drained the accumulator (acc_empty)
+// before the next segment's first MMA.
 template <int BN, bool SPLIT3, bool SK>
 __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
