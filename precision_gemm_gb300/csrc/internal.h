@@ -27,6 +27,7 @@ struct GemmParams {
     int32_t split;           // number of slices
     int32_t group_m;         // rasterisation: tile rows per group
     int32_t c_vec;           // C 16-byte aligned and ldc % 4 == 0
+    int32_t c_tma;           // FFMA: whole-tile CTAs store C through the tensor map tmC (beta = 0, split 1)
     int32_t debug_flags;
     int32_t a3d;             // tcgen05 kernels: A tensor map is 3-D {32, k, m/32} (one box per 128 rows)
     int32_t a_kmajor;        // tcgen05 kernels: A is read K-major (transa = 'T'), else M-major
@@ -63,7 +64,7 @@ int ffma_threads(int bn);
 int ffma_stages(int bn);
 int ffma_ctas_per_sm(int bn);
 size_t ffma_smem_bytes(int bn);
-cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+cudaError_t launch_ffma(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
                         int bn, dim3 grid, cudaStream_t stream);
 // FFMA stream-K (bn in {64, 128}): `ctas` co-resident CTAs share the product's
 // (tile, k-block) iterations; then the fix-up kernel adds each tile's partial

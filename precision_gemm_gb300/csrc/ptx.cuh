@@ -234,6 +234,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 2-D tiled store of the shared-memory box at `src` to (x, y) of the tensor (x
+// contiguous, a multiple of 4 elements, never negative); elements of the box
+// outside the tensor are not written.  Completes through the bulk-group
+// mechanism: bulk_commit() then bulk_wait_read() before `src` may be reused or
+// the CTA may exit.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // ---- tcgen05 -----------------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {

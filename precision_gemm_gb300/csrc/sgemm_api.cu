@@ -40,6 +40,11 @@ namespace {
 
 // Tile rows per rasterisation group (a compile-time tunable; 4, 8 and 16 measured
 // within noise of each other at 8192^3).
+// FFMA: whole-tile results with beta = 0 leave through TMA stores (1) or
+// through thread stores of whole columns (0).
+#ifndef PG_FFMA_TMA_STORE
+#define PG_FFMA_TMA_STORE 1
+#endif
 #ifndef PG_GROUP_M
 #define PG_GROUP_M 16
 #endif
@@ -562,10 +567,18 @@ int launch_gemm(const sgemm_plan_t& pl, bool split3, bool a_kmajor, bool b_mnmaj
                         static_cast<unsigned>(pl.split_k));
         if ((rc = encode_2d(&tmA, a_big, m, k, pl.ld_a, kBM, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))) return rc;
         if ((rc = encode_2d(&tmB, b_big, k, n, pl.ld_b, kFfmaBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+        // C by TMA stores (boxes of 32 rows x bn columns, 128-byte swizzle) when
+        // the tile's result is final and needs no read of C.
+        CUtensorMap tmC{};
+        gp.c_tma = 0;
+        if (PG_FFMA_TMA_STORE && pl.sk_ctas == 0 && gp.split == 1 && gp.beta == 0.0f && gp.c_vec) {
+            if ((rc = encode_2d(&tmC, gp.C, m, n, gp.ldc, 32, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+            gp.c_tma = 1;
+        }
         if (pl.sk_ctas > 0) {
             if ((e = launch_ffma_sk(tmA, tmB, gp, pl.bn, pl.sk_ctas, num_sms, st)) != cudaSuccess)
                 return fail_cuda(e, "FFMA stream-K kernels");
-        } else if ((e = launch_ffma(tmA, tmB, gp, pl.bn, grid, st)) != cudaSuccess) {
+        } else if ((e = launch_ffma(tmA, tmB, tmC, gp, pl.bn, grid, st)) != cudaSuccess) {
             return fail_cuda(e, "FFMA GEMM kernel");
         }
     } else {
