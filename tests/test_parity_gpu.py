@@ -432,6 +432,31 @@ def test_subnormal_operands(mode, mnk):
     assert np.all(got[0:8, 13:20] != 0)
 
 
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("m,ldc", [(1, 4), (31, 36), (33, 36), (100, 104), (160, 164), (167, 172), (256, 256),
+                                   (167, 171)])
+@pytest.mark.parametrize("beta,split", [(0.0, 1), (0.75, 1), (0.0, 3)])
+def test_ffma_epilogue_paths(bn, m, ldc, beta, split):
+    """The FFMA epilogue of a CTA that owns its tile or K slice: with beta = 0 and
+    C 16-byte aligned with ldc % 4 == 0 the tile leaves as TMA boxes of 32 rows
+    (the box that m cuts is stored by the threads); otherwise, or with K split,
+    the threads store whole columns from the staged tile.  Rows cut inside a
+    box, columns cut inside a tile, every tile width; every entry against the
+    oracle, the ld gaps and the canaries untouched."""
+    p = synth.Problem(m, 200, 70, ldc=ldc, alpha=-1.5, beta=beta, dist="normal", seed=31 + m)
+    A, B, C = synth.make(p)
+    try:
+        pg.force_plan(bn, split)
+        out, canaries = H.run_gpu(p, "ffma", A, B, C)
+    finally:
+        pg.force_plan(0, 0)
+    cref, den = H.reference_full(p, A, B, C)
+    res = oracle.check(H.logical(p, out), cref, den, oracle.TOL["ffma"])
+    assert res["ok"], res
+    assert canaries and H.padding_intact(p, out, C)
+    assert pg.device_status() == 0
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_beta_zero_ignores_nan_c(mode):
     p = synth.Problem(200, 150, 100, alpha=1.0, beta=0.0, dist="normal", seed=17)
