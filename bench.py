@@ -269,21 +269,26 @@ def run_ours(args, wl_name):
                 stream.wait_stream(hstreams[mode])
         for _ in range(max(1, min(args.warmup, 2))):
             host_step()
-        e_steps = max(1, min(args.steps, 3))
+        # each step timed on its own (events on the launching stream); the median
+        # step stands for the run, the slowest and fastest are reported beside it
+        e_steps = max(1, min(args.steps, 5))
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e_ms = []
         for _ in range(e_steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
             host_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        te = torch.tensor([e0.elapsed_time(e1) / e_steps], dtype=torch.float64, device="cuda")
+            e1.record(stream)
+            e1.synchronize()
+            e_ms.append(e0.elapsed_time(e1))
+        te = torch.tensor([statistics.median(e_ms)], dtype=torch.float64, device="cuda")
         if dist:
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
         e2e = {"value": world * flops * len(modes) / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "ms_per_step": float(te.item()), "ms_min": min(e_ms), "ms_max": max(e_ms),
                "api": "sgemm_host_async, one stream per mode (pinned host buffers)"}
 
     # The hybrid CPU + GPU column split, end to end through the synchronous host
