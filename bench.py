@@ -46,6 +46,8 @@ WORKLOADS = {
                      synth.Problem(4096, 4096, 4096, alpha=1.0, beta=0.0, dist="uniform", seed=0, layout="row")),
     "rowmajor2048": ("sgemm row-major 2048^3, alpha=1 beta=0, A,B ~ U[-1,1) seed 0",
                      synth.config_problems()["c2_rm2048"]),
+    "rowmajor1024": ("sgemm row-major 1024^3, alpha=1 beta=0, A,B ~ U[-1,1) seed 0",
+                     synth.config_problems()["c2_rm1024"]),
     "ragged": ("sgemm column-major 3000x1500x777, lda=3013 ldb=784 ldc=3005, alpha=1.5 beta=-0.5, N(0,1)",
                synth.config_problems()["c3_ragged"]),
     "skinny_k64": ("sgemm column-major 16384x16384x64, N(0,1)", synth.config_problems()["c5a_16384x16384x64"]),
