@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(256, SPLIT ? 3 : 4)
     prep_copy_kernel(const float* __restrict__ src, int64_t lds, int64_t rows, int64_t cols,
                      float* __restrict__ dst, float* __restrict__ dst_small, int64_t ldd, int tx_shift,
                      int by_rows) {
+    pdl_wait();  // launched after the other operand's pass: that pass's completion
+    if (threadIdx.x == 0) pdl_trigger();  // the GEMM may be scheduled; it waits for this pass
     const Sweep w = sweep_setup(tx_shift);
     float x[kU];
     sweep_batches(
@@ -114,6 +116,8 @@ template <bool SPLIT>
 __global__ void __launch_bounds__(256) prep_copy_vec_kernel(const float* __restrict__ src, int64_t lds, int64_t rows,
                                                             int64_t cols, float* __restrict__ dst,
                                                             float* __restrict__ dst_small, int64_t ldd) {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const int64_t rq = (rows + 3) / 4;  // chunks per column
     const int64_t total = rq * cols;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -171,6 +175,8 @@ __global__ void __launch_bounds__(256) prep_transpose_kernel(const float* __rest
                                                              float* __restrict__ dst,
                                                              float* __restrict__ dst_small, int64_t ldd) {
     __shared__ float tile[32][33];
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const int64_t tiles_r = (rows + 31) / 32;
     const int64_t tiles_c = (cols + 31) / 32;
     for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
@@ -212,6 +218,7 @@ constexpr int kS = 8;
 // chunk is whole, else element by element.  Rows from m up to ldp of P are
 // loaded with the chunk but never stored.
 __global__ void __launch_bounds__(256) splitk_reduce_vec_kernel(const GemmParams p) {
+    pdl_wait();  // the GEMM's partial sums
     const int64_t rq = (p.m + 3) / 4;
     const int64_t total = rq * p.n;
     const int64_t st4 = p.p_stride / 4;
@@ -319,6 +326,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_grouped_kernel(const GemmPa
 // with ldc % 4 == 0 and the 4 rows lie inside C.
 template <int BN>
 __global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmParams p, int G) {
+    pdl_wait();  // the stream-K kernel's partial blocks
     constexpr int BM = kBM;
     constexpr int RQ = BM / 4;       // float4 chunks per tile column
     constexpr int CH = RQ * BN;      // per tile
@@ -419,19 +427,19 @@ dim3 sweep_grid(int64_t rows, int64_t cols, int num_sms, int* tx_shift, int* by_
 }  // namespace
 
 cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t rows, int64_t cols, float* dst,
-                        float* dst_small, int64_t ldd, int num_sms, cudaStream_t stream) {
+                        float* dst_small, int64_t ldd, int num_sms, cudaStream_t stream, bool after_previous) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const bool dep = PG_PDL_PREP && after_previous;
     if (transposed) {
         const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
         int64_t g = static_cast<int64_t>(num_sms) * 8;
         if (g > tiles) g = tiles;
         const dim3 block(32, 8);
         if (dst_small)
-            prep_transpose_kernel<true><<<static_cast<unsigned>(g), block, 0, stream>>>(src, lds, rows, cols, dst,
-                                                                                        dst_small, ldd);
-        else
-            prep_transpose_kernel<false><<<static_cast<unsigned>(g), block, 0, stream>>>(src, lds, rows, cols,
-                                                                                         dst, nullptr, ldd);
+            return launch_kernel(dep, prep_transpose_kernel<true>, dim3(static_cast<unsigned>(g)), block, 0, stream,
+                                 src, lds, rows, cols, dst, dst_small, ldd);
+        return launch_kernel(dep, prep_transpose_kernel<false>, dim3(static_cast<unsigned>(g)), block, 0, stream, src,
+                             lds, rows, cols, dst, static_cast<float*>(nullptr), ldd);
     } else if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && lds % 4 == 0 &&
                (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && ldd % 4 == 0 &&
                (dst_small == nullptr || (reinterpret_cast<uintptr_t>(dst_small) & 15u) == 0)) {
@@ -440,21 +448,18 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
         const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
         if (g > cap) g = cap;
         if (dst_small)
-            prep_copy_vec_kernel<true><<<static_cast<unsigned>(g), 256, 0, stream>>>(src, lds, rows, cols, dst,
-                                                                                    dst_small, ldd);
-        else
-            prep_copy_vec_kernel<false><<<static_cast<unsigned>(g), 256, 0, stream>>>(src, lds, rows, cols, dst,
-                                                                                     nullptr, ldd);
-    } else {
-        int sh = 8, by_rows = 0;
-        const dim3 grid = sweep_grid(rows, cols, num_sms, &sh, &by_rows);
-        if (dst_small)
-            prep_copy_kernel<true>
-                <<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, dst_small, ldd, sh, by_rows);
-        else
-            prep_copy_kernel<false><<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, nullptr, ldd, sh, by_rows);
+            return launch_kernel(dep, prep_copy_vec_kernel<true>, dim3(static_cast<unsigned>(g)), dim3(256), 0,
+                                 stream, src, lds, rows, cols, dst, dst_small, ldd);
+        return launch_kernel(dep, prep_copy_vec_kernel<false>, dim3(static_cast<unsigned>(g)), dim3(256), 0, stream,
+                             src, lds, rows, cols, dst, static_cast<float*>(nullptr), ldd);
     }
-    return cudaGetLastError();
+    int sh = 8, by_rows = 0;
+    const dim3 grid = sweep_grid(rows, cols, num_sms, &sh, &by_rows);
+    if (dst_small)
+        return launch_kernel(dep, prep_copy_kernel<true>, grid, dim3(256), 0, stream, src, lds, rows, cols, dst,
+                             dst_small, ldd, sh, by_rows);
+    return launch_kernel(dep, prep_copy_kernel<false>, grid, dim3(256), 0, stream, src, lds, rows, cols, dst,
+                         static_cast<float*>(nullptr), ldd, sh, by_rows);
 }
 
 cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t stream) {
@@ -465,6 +470,9 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t 
         int64_t bx = (target + by - 1) / by;
         if (bx > row_blocks) bx = row_blocks;
         if (bx < 1) bx = 1;
+        // An ordinary launch: dependent-launched, its few long-running CTAs were
+        // placed beside the GEMM's on the SMs that had room and ran slower (128 x
+        // 128 x 262144 TF32 0.066 -> 0.068 ms); the other reductions gain.
         splitk_reduce_grouped_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by)), 256, 0, stream>>>(
             p);
         return cudaGetLastError();
@@ -475,8 +483,7 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t 
     int64_t g = (chunks + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
     if (g > cap) g = cap;
-    splitk_reduce_vec_kernel<<<static_cast<unsigned>(g), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_after_previous(splitk_reduce_vec_kernel, dim3(static_cast<unsigned>(g)), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_streamk_fixup(const GemmParams& p, int bn, int ctas, int num_sms, cudaStream_t stream) {
@@ -485,11 +492,14 @@ cudaError_t launch_streamk_fixup(const GemmParams& p, int bn, int ctas, int num_
     const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
     if (g > cap) g = cap;
     switch (bn) {
-        case 64: streamk_fixup_kernel<64><<<static_cast<unsigned>(g), 256, 0, stream>>>(p, ctas); break;
-        case 128: streamk_fixup_kernel<128><<<static_cast<unsigned>(g), 256, 0, stream>>>(p, ctas); break;
+        case 64:
+            return launch_after_previous(streamk_fixup_kernel<64>, dim3(static_cast<unsigned>(g)), dim3(256), 0, stream,
+                                         p, ctas);
+        case 128:
+            return launch_after_previous(streamk_fixup_kernel<128>, dim3(static_cast<unsigned>(g)), dim3(256), 0,
+                                         stream, p, ctas);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_scale(float* C, int64_t ldc, int64_t m, int64_t n, float beta, int num_sms,

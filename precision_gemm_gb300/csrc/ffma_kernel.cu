@@ -280,6 +280,7 @@ template <int BN, int JJ>
 __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTAS_PER_SM)
     ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    if (PG_PDL_EARLY && threadIdx.x == 0) pdl_trigger();
     using Cfg = FfmaCfg<BN, JJ>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -320,6 +321,7 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // launched right after an operand pass: its output, before any copy
 
     // Thread 0 is also the loader: it issues k-block `it` into slot it % S once
     // every warp has released that slot's previous contents (k-block it - S).
@@ -405,6 +407,8 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
+    // the main loop is done: a dependent reduction may be scheduled now
+    if (!PG_PDL_EARLY && threadIdx.x == 0) pdl_trigger();
     if (loader) {
         // The last (up to S) slots issued may still be landing after an abort; do
         // not let the CTA retire while a copy into its shared memory is in flight.
@@ -565,6 +569,7 @@ template <int BN, int JJ>
 __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTAS_PER_SM)
     ffma_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
+    if (PG_PDL_EARLY && threadIdx.x == 0) pdl_trigger();
     using Cfg = FfmaCfg<BN, JJ>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -622,6 +627,7 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
         ld_kb = 0;
     }
     __syncthreads();
+    pdl_wait();  // launched right after an operand pass: its output, before any copy
     const int n_it = n_its;
 
     // Thread 0 is also the loader, PD k-blocks ahead of the consumers.
@@ -696,6 +702,8 @@ __global__ void __launch_bounds__(FfmaCfg<BN, JJ>::THREADS, FfmaCfg<BN, JJ>::CTA
             if (++seg < n_segs) left = seg_len[seg];
         }
     }
+    // the main loop is done: the fix-up may be scheduled now
+    if (!PG_PDL_EARLY && threadIdx.x == 0) pdl_trigger();
     if (loader) {
         for (int g = max(0, issued - S); g < issued; ++g)
             mbar_wait_bounded(full0 + 8 * (g % S), (g / S) & 1, p.timeout_ns, nullptr);
@@ -710,8 +718,9 @@ cudaError_t launch_sk_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    kern<<<ctas, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_kernel(p.after_prep != 0, kern, dim3(ctas), dim3(Cfg::THREADS), Cfg::SMEM, stream, tmA, tmB, p)) !=
+        cudaSuccess)
+        return e;
     return launch_streamk_fixup(p, BN, ctas, num_sms, stream);
 }
 
@@ -723,8 +732,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, tmC, p);
-    return cudaGetLastError();
+    return launch_kernel(p.after_prep != 0, kern, grid, dim3(Cfg::THREADS), Cfg::SMEM, stream, tmA, tmB, tmC, p);
 }
 
 using Cfg64 = FfmaCfg<64, 8>;

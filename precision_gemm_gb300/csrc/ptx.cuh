@@ -203,6 +203,24 @@ __device__ __forceinline__ void split_tile_in_place(uint8_t* tile, uint8_t* smal
     }
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// In a kernel launched with launch_after_previous: block until the previous
+// kernel in the stream has completed and its memory operations are visible.
+// Returns at once in a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let a dependent kernel (launched with launch_after_previous) be scheduled
+// once every CTA of this grid has issued this or exited.  The dependent still
+// waits for this grid's completion before it reads anything.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Where the GEMM kernels let their dependent kernel be scheduled: at their
+// start (1), or once their main loop has issued its last copy (0).
+#ifndef PG_PDL_EARLY
+#define PG_PDL_EARLY 0
+#endif
+
 // ---- TMA -----------------------------------------------------------------------
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -675,7 +675,7 @@ int prepare_a(const sgemm_plan_t& pl, char transa, int64_t m, int64_t k, const f
                      : nullptr;
     const bool tr = pl.prep_a == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into M-major
     const bool kmaj = !tr && !is_notrans(transa);      // tensor cores: stored k x m, kept as is
-    cudaError_t e = launch_prep(A, lda, tr, kmaj ? k : m, kmaj ? m : k, d, ds2, pl.ld_a, num_sms, st);
+    cudaError_t e = launch_prep(A, lda, tr, kmaj ? k : m, kmaj ? m : k, d, ds2, pl.ld_a, num_sms, st, false);
     if (e != cudaSuccess) return fail_cuda(e, "operand preparation (A)");
     out->big = d;
     out->small = ds2;
@@ -713,12 +713,14 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
 
     const float* a_big = A;
     const float* a_small = nullptr;
+    bool a_prepped = false;  // this call launched A's pass
     if (a_given) {
         a_big = pre->big;
         a_small = pre->small;
     } else if (a_prep > 0) {
         PreparedA pa;
         if ((rc = prepare_a(pl, transa, m, k, A, lda, cursor, ds->sms, st, &pa))) return rc;
+        a_prepped = true;
         cursor += a_prep;
         a_big = pa.big;
         a_small = pa.small;
@@ -736,7 +738,8 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
         }
         const bool tr = pl.prep_b == SGEMM_PREP_TRANSPOSE;  // FFMA only: transposed into K-major
         const bool nmaj = !tr && !is_notrans(transb);      // tensor cores: stored n x k, kept as is
-        if ((e = launch_prep(B, ldb, tr, nmaj ? n : k, nmaj ? k : n, d, ds2, pl.ld_b, ds->sms, st)) != cudaSuccess)
+        if ((e = launch_prep(B, ldb, tr, nmaj ? n : k, nmaj ? k : n, d, ds2, pl.ld_b, ds->sms, st, a_prepped)) !=
+            cudaSuccess)
             return fail_cuda(e, "operand preparation (B)");
         b_big = d;
         b_small = ds2;
@@ -783,6 +786,8 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
     gp.debug_flags = g_debug.load();
     gp.timeout_ns = g_timeout_ns.load();
     gp.status = ds->status;
+    // the GEMM right after this call's operand pass (no memset between them)
+    gp.after_prep = (PG_PDL_PREP && (a_prepped || pl.prep_b != SGEMM_PREP_NONE) && pl.tail_split <= 1) ? 1 : 0;
 
     const bool tcm = pl.kernel != SGEMM_KERNEL_FFMA;
     return launch_gemm(pl, split3, tcm && !is_notrans(transa), tcm && !is_notrans(transb), a_big, a_small, b_big,

@@ -169,6 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
                     const GemmParams p) {
+    if (PG_PDL_EARLY && threadIdx.x == 0) pdl_trigger();
     using Cfg = Tc2Cfg<BN, SPLIT3>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -217,6 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
     cluster_sync_all();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
+    pdl_wait();  // launched right after an operand pass: its output, before any copy
 
     // Work unit -> (pair tile t, K slice, k-block range).
     auto unit_geometry = [&](int u, int64_t& m0, int64_t& n0, int& slice, int& kb0, int& nkb, int& t) {
@@ -326,6 +328,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN, SPLIT3>::
                     load_b(b_slot, &tmB);
                 }
             }
+            // every copy of the main loop is issued: a dependent reduction may be
+            // scheduled now
+            if (!PG_PDL_EARLY) pdl_trigger();
             if (leader) {
                 // Let every copy of the pair land before the CTAs may retire (CTA 0's
                 // full barriers count both CTAs' bytes).
@@ -592,8 +597,8 @@ struct Launcher {
         int pairs = units < max_clusters ? units : max_clusters;
         if (pairs < 1) pairs = 1;
         *pairs_out = pairs;
-        kern<<<dim3(2 * pairs), Cfg::THREADS, Cfg::SMEM, st>>>(a, as, b, bs, p);
-        return cudaGetLastError();
+        return launch_kernel(p.after_prep != 0, kern, dim3(2 * pairs), dim3(Cfg::THREADS), Cfg::SMEM, st, a, as, b, bs,
+                             p);
     }
 };
 

@@ -162,6 +162,7 @@ template <int BN, bool SPLIT3, bool SK>
 __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBs, const GemmParams p) {
+    if (PG_PDL_EARLY && threadIdx.x == 0) pdl_trigger();
     using Cfg = TcCfg<BN, SPLIT3>;
     static_assert(!SK || (SPLIT3 && Cfg::FUSED && Cfg::KPS == 1), "stream-K: fused 3xTF32, one k-block per slot");
     constexpr int S = Cfg::STAGES;
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
+    pdl_wait();  // launched right after an operand pass: its output, before any copy
     // ring slots' worth of k-blocks; the last may hold fewer
     const int nst = SK ? sk_nits : (nkb + KPS - 1) / KPS;
 
@@ -322,6 +324,9 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT3>::THREADS, 1)
                     issued = it + 1;
                 }
             }
+            // every copy of the main loop is issued: a dependent reduction or fix-up
+            // may be scheduled now
+            if (!PG_PDL_EARLY) pdl_trigger();
             // Let every copy this CTA issued land before it may retire.
             for (int it = max(0, issued - S); it < issued; ++it)
                 mbar_wait_bounded(full0 + 8 * (it % S), (it / S) & 1, p.timeout_ns, nullptr);
@@ -598,8 +603,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(tmA, tmB, tmBs, p);
-    return cudaGetLastError();
+    return launch_kernel(p.after_prep != 0, kern, grid, dim3(Cfg::THREADS), Cfg::SMEM, stream, tmA, tmB, tmBs, p);
 }
 
 template <bool SPLIT3>
