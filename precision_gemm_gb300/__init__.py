@@ -138,37 +138,39 @@ def _ptr(x) -> int:
     raise TypeError("cannot take a pointer from %r" % type(x))
 
 
-def _notrans(t) -> bool:
-    return _tchar(t) in (b"N", b"n")
+_torch = None
 
 
-def _extent(rows: int, cols: int, ld: int) -> int:
-    """Elements from the first one that a rows x cols column-major operand with
-    leading dimension ld spans (the last column needs only its rows)."""
-    return 0 if rows <= 0 or cols <= 0 else ld * (cols - 1) + rows
+def _torch_mod():
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
 
 
-def _check_operand(x, name: str, rows: int, cols: int, ld: int, on_device: bool) -> None:
+def _check_operand(x, name: str, rows: int, cols: int, ld: int, on_device: bool, cur_dev=None) -> None:
     """Raise ValueError unless tensor / array x can serve as a rows x cols operand
     with leading dimension ld: float32, in device memory of the current CUDA
-    device (on_device) or in host memory (not on_device), with storage for the
-    whole extent.  ints are not checked; None is left to the library, which
-    rejects a null pointer the call needs."""
+    device (on_device; cur_dev is that device's index when the caller has it) or
+    in host memory (not on_device), with storage for the whole extent.  ints are
+    not checked; None is left to the library, which rejects a null pointer the
+    call needs."""
     if x is None or isinstance(x, int):
         return
-    if hasattr(x, "untyped_storage"):  # torch tensor
-        import torch
+    torch = _torch_mod()
+    if isinstance(x, torch.Tensor):
         if x.dtype != torch.float32:
             raise ValueError("%s: expected a float32 tensor, got %s" % (name, x.dtype))
         if on_device:
             if not x.is_cuda:
                 raise ValueError("%s: expected a CUDA tensor, got one on %s" % (name, x.device))
-            cur = torch.cuda.current_device()
-            if x.device.index != cur:
+            cur = torch.cuda.current_device() if cur_dev is None else cur_dev
+            if x.get_device() != cur:
                 raise ValueError("%s: the tensor is on %s, the current device is cuda:%d" % (name, x.device, cur))
         elif x.is_cuda:
             raise ValueError("%s: expected a host (CPU) tensor, got one on %s" % (name, x.device))
-        avail = (x.untyped_storage().nbytes() - x.storage_offset() * x.element_size()) // 4
+        avail = (x.untyped_storage().nbytes() - x.storage_offset() * 4) // 4
     elif hasattr(x, "ctypes") and hasattr(x, "dtype"):  # numpy array
         if on_device:
             raise ValueError("%s: a numpy array is host memory; this call takes device memory" % name)
@@ -181,7 +183,7 @@ def _check_operand(x, name: str, rows: int, cols: int, ld: int, on_device: bool)
         raise TypeError("%s: cannot take a pointer from %r" % (name, type(x)))
     if ld < max(1, rows):
         return  # the library reports the bad leading dimension as an invalid argument
-    need = _extent(rows, cols, ld)
+    need = 0 if rows <= 0 or cols <= 0 else ld * (cols - 1) + rows  # the last column needs only its rows
     if avail < need:
         raise ValueError("%s: a %d x %d operand with leading dimension %d spans %d elements; the storage from the "
                          "tensor's first element holds %d" % (name, rows, cols, ld, need, avail))
@@ -192,19 +194,22 @@ def _check_gemm_operands(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C
     the call reads or writes it (the library's own rules for what it touches)."""
     if m <= 0 or n <= 0:
         return
+    cur = None
+    if on_device and any(getattr(x, "is_cuda", False) for x in (A, B, C)):
+        cur = _torch_mod().cuda.current_device()
     reads_ab = k > 0 and alpha != 0.0
     if reads_ab:
-        ra, ca = (m, k) if _notrans(transa) else (k, m)
-        rb, cb = (k, n) if _notrans(transb) else (n, k)
-        _check_operand(A, "A", ra, ca, lda, on_device)
-        _check_operand(B, "B", rb, cb, ldb, on_device)
+        ra, ca = (m, k) if transa in ("N", "n", b"N", b"n") else (k, m)
+        rb, cb = (k, n) if transb in ("N", "n", b"N", b"n") else (n, k)
+        _check_operand(A, "A", ra, ca, lda, on_device, cur)
+        _check_operand(B, "B", rb, cb, ldb, on_device, cur)
     if reads_ab or beta != 1.0:
-        _check_operand(C, "C", m, n, ldc, on_device)
+        _check_operand(C, "C", m, n, ldc, on_device, cur)
 
 
 def _stream(s) -> int:
     if s is None:
-        import torch
+        torch = _torch_mod()
         return int(torch.cuda.current_stream().cuda_stream) if torch.cuda.is_available() else 0
     if isinstance(s, int):
         return s
