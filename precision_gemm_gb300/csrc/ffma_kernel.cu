@@ -715,8 +715,8 @@ cudaError_t launch_sk_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            int num_sms, cudaStream_t stream) {
     using Cfg = FfmaCfg<BN, JJ>;
     auto kern = ffma_sk_kernel<BN, JJ>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::SMEM));
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = set_smem_limit_once(smem_set, reinterpret_cast<const void*>(kern), static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
     if ((e = launch_kernel(p.after_prep != 0, kern, dim3(ctas), dim3(Cfg::THREADS), Cfg::SMEM, stream, tmA, tmB, p)) !=
         cudaSuccess)
@@ -729,8 +729,8 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
                         dim3 grid, cudaStream_t stream) {
     using Cfg = FfmaCfg<BN, JJ>;
     auto kern = ffma_gemm_kernel<BN, JJ>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::SMEM));
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = set_smem_limit_once(smem_set, reinterpret_cast<const void*>(kern), static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
     return launch_kernel(p.after_prep != 0, kern, grid, dim3(Cfg::THREADS), Cfg::SMEM, stream, tmA, tmB, tmC, p);
 }

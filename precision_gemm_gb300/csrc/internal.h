@@ -3,6 +3,7 @@
 
 #include <cuda.h>  // CUtensorMap (header only; the driver is reached at run time)
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 namespace pg {
@@ -48,6 +49,21 @@ template <typename... Params, typename... Args>
 cudaError_t launch_after_previous(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                                   Args... args) {
     return launch_kernel(PG_PDL != 0, kern, grid, block, smem, st, args...);
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` once per device:
+// the attribute stays set for the process, and setting it on every launch cost
+// a driver call per call.  `done` holds one bit per device ordinal (a static of
+// the launcher instantiation that owns the kernel).
+inline cudaError_t set_smem_limit_once(std::atomic<uint64_t>& done, const void* kern, int bytes) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const uint64_t bit = uint64_t(1) << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 // Tile geometry common to every GEMM kernel: BM rows of C per CTA.

@@ -507,6 +507,62 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// A tensor map depends only on the arguments it is encoded from, so the maps of
+// repeated calls on the same buffers are kept instead of re-encoded (a driver
+// call each, two to four per product): a direct-mapped table of 256 entries,
+// each with the arguments it was made from.
+struct MapKey {
+    const void* base;
+    uint32_t rank;
+    int32_t swizzle;
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[256];
+
+CUresult encode_cached(EncodeTiledFn fn, CUtensorMap* map, uint32_t rank, const float* base, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+    MapKey key;
+    std::memset(&key, 0, sizeof key);  // padding included: keys compare as bytes
+    key.base = base;
+    key.rank = rank;
+    key.swizzle = static_cast<int32_t>(swizzle);
+    for (uint32_t i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+    const unsigned char* kb = reinterpret_cast<const unsigned char*>(&key);
+    for (size_t i = 0; i < sizeof key; ++i) h = (h ^ kb[i]) * 1099511628211ull;
+    MapEntry& slot = g_maps[h & 255];
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        if (slot.valid && std::memcmp(&slot.key, &key, sizeof key) == 0) {
+            *map = slot.map;
+            return CUDA_SUCCESS;
+        }
+    }
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<float*>(base), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        slot.key = key;
+        slot.map = *map;
+        slot.valid = true;
+    }
+    return r;
+}
+
 // An M/N-major operand (rows x cols, leading dimension ld, rows % 32 == 0) as the
 // 3-D tensor {32 rows, cols, rows / 32} with box {32, box_cols, groups}: one copy
 // fetches 32 * groups rows as `groups` [box_cols][32] row groups, the layout that
@@ -521,10 +577,7 @@ int encode_mn3d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols,
     const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows / 32)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, 32 * 4};
     const cuuint32_t box[3] = {32, box_cols, groups};
-    const cuuint32_t elem[3] = {1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
-                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = encode_cached(fn, map, 3, base, dims, strides, box, swizzle);
     if (r != CUDA_SUCCESS)
         return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled (3-D) failed (%d) for a %lld x %lld matrix, ld %lld",
                     static_cast<int>(r), (long long)rows, (long long)cols, (long long)ld);
@@ -542,10 +595,7 @@ int encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, i
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
     const cuuint32_t box[2] = {box_rows, box_cols};
-    const cuuint32_t elem[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
-                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = encode_cached(fn, map, 2, base, dims, strides, box, swizzle);
     if (r != CUDA_SUCCESS)
         return fail(SGEMM_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld matrix, ld %lld",
                     static_cast<int>(r), (long long)rows, (long long)cols, (long long)ld);

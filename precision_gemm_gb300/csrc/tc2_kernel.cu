@@ -573,8 +573,9 @@ struct Launcher {
                            const GemmParams& p, int units, int num_sms, cudaStream_t st, int* pairs_out) {
         using Cfg = Tc2Cfg<BN, SPLIT3>;
         auto kern = tc2_gemm_kernel<BN, SPLIT3>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(Cfg::SMEM));
+        static std::atomic<uint64_t> smem_set{0};
+        cudaError_t e =
+            set_smem_limit_once(smem_set, reinterpret_cast<const void*>(kern), static_cast<int>(Cfg::SMEM));
         if (e != cudaSuccess) return e;
         // Pairs that can be resident at once (clusters must fit inside GPCs), asked
         // once per device so a call captured into a CUDA graph only launches.
