@@ -33,7 +33,8 @@
 //     CTA keeps the per-thread epilogue (its warps finish one by one).
 //
 // Tile shapes: 128 x 128 (256 threads, 3 slots, two CTAs per SM) is the default;
-// 128 x 64 serves n <= 64 and 128 x 256 (512 threads, 4 slots) stays selectable.
+// 128 x 64 (128 threads, 3 slots, three CTAs per SM) serves n <= 64 and tiny
+// products, and 128 x 256 (512 threads, 4 slots) stays selectable.
 // Measured on GB300 at 8192^3: 128 x 128 with float2 B reads and PD = 1 runs at
 // 62.7 TFLOP/s against 58.7 for 128 x 256 with float4 B reads.
 //
@@ -67,13 +68,17 @@ struct FfmaCfg {
     static constexpr int TGN = BN / JJ;                   // thread columns (JJ columns per thread)
     static constexpr int THREADS = 16 * TGN;              // 16 thread rows x TGN
     static constexpr int CWARPS = THREADS / 32;
-    static constexpr int STAGES = (BN == 128) ? 3 : 4;
+    static constexpr int STAGES = (BN == 256) ? 4 : 3;
     // While k-block `it` is computed, thread 0 issues k-block it + PD into slot
     // (it + PD) % STAGES, whose previous contents (k-block it + PD - STAGES) every
     // warp released STAGES - PD iterations ago; with a spare slot (PD = STAGES-2)
     // the loader waits only if some warp trails by two whole k-blocks.
     static constexpr int PD = STAGES - 2;
-    static constexpr int CTAS_PER_SM = (BN == 256) ? 1 : 2;
+    // 128 x 64 tiles run three CTAs per SM (12 warps; 74.8 KB of shared memory
+    // and up to 170 registers each): against two CTAs with four slots, 8192 x 64 x
+    // 8192 0.1686 -> 0.1604 ms, 16384 x 64 x 16384 0.627 -> 0.603, 8192 x 32 x
+    // 8192 0.169 -> 0.158 (2048 x 64 x 16384 0.0887 -> 0.0908).
+    static constexpr int CTAS_PER_SM = (BN == 256) ? 1 : (BN == 64 ? 3 : 2);
     static constexpr int A_BYTES = BM * BK * 4;           // 16 KiB
     static constexpr int B_BYTES = BN * BK * 4;           // BN rows of 128 B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;

@@ -264,7 +264,7 @@ def test_last_wave_split_ffma(mnk):
 
 
 @pytest.mark.parametrize("mnk,ldc_pad,beta", [((2048, 2048, 2048), 3, 0.5), ((1000, 1300, 4000), 0, -1.0),
-                                               ((1024, 1024, 8192), 4, 0.0), ((8192, 64, 8192), 1, 1.5),
+                                               ((1024, 1024, 8192), 4, 0.0), ((12000, 50, 5200), 1, 1.5),
                                                ((1100, 700, 6000), 2, 0.25), ((1250, 1650, 5000), 0, 0.0)])
 def test_ffma_stream_k(mnk, ldc_pad, beta):
     """FFMA products whose tiles fill less than one wave of CTA slots run stream-K:
