@@ -195,7 +195,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // K split stream A faster).
     // Tiny FFMA products (under 2 GFLOP, their 128 x 64 tiles filling at most half
     // the SMs) take the 64-wide tile too, with thinner K slices below: more CTAs
-    // share the few k-blocks.
+    // share the few k-blocks; so do FFMA products with K <= 64 (below).
     int bn = n <= 64 ? 64 : ((n <= 128 || !tc) ? 128 : 256);
     const int64_t tiles64 = cdiv(m, kBM) * cdiv(n, 64);
     const bool one_wave64 = tc && tiles64 <= std::max(num_sms, 1);
@@ -216,6 +216,11 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     if (single128) bn = 128;
     const bool tiny_ffma = !tc && 2 * tiles64 <= std::max(num_sms, 1) && 2.0 * m * n * k <= 2e9;
     if (tiny_ffma) bn = 64;
+    // FFMA with at most two k-blocks (K <= 64): a CTA's prologue and epilogue weigh
+    // as much as its arithmetic, and three 128 x 64 CTAs per SM overlap them better
+    // than two 128 x 128 ones: 16384^2 x 64 0.654 -> 0.611 ms, 16384^2 x 32 0.422 ->
+    // 0.345, 8192^2 x 64 0.169 -> 0.158 (K = 128 1 % slower, K = 256 even).
+    if (!tc && k <= 2 * kFfmaBK) bn = 64;
     // TF32 on SM pairs: 256 x 512 tiles (two N = 256 MMAs per k-step) need 48 B/clk
     // per SM of operand feed at the full MMA rate against 64 for 256 x 256 tiles
     // (bulk copies sustain ~65 per SM), at the price of a single TMEM accumulator
