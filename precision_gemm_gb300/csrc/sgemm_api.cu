@@ -168,7 +168,7 @@ size_t tail_counter_bytes(const sgemm_plan_t& pl) {
 // (the allocation-free entry) never plans a last-wave split.
 void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, const void* A,
                int64_t lda, const void* B, int64_t ldb, float beta, int mode, int num_sms, sgemm_plan_t* pl,
-               bool allow_tail = true) {
+               bool allow_tail = true, int ffma_bn = 0) {
     std::memset(pl, 0, sizeof *pl);
     pl->mode = mode;
     pl->split_k = 1;
@@ -221,6 +221,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // than two 128 x 128 ones: 16384^2 x 64 0.654 -> 0.611 ms, 16384^2 x 32 0.422 ->
     // 0.345, 8192^2 x 64 0.169 -> 0.158 (K = 128 1 % slower, K = 256 even).
     if (!tc && k <= 2 * kFfmaBK) bn = 64;
+    if (ffma_bn) bn = ffma_bn;  // the re-plan below
     // TF32 on SM pairs: 256 x 512 tiles (two N = 256 MMAs per k-step) need 48 B/clk
     // per SM of operand feed at the full MMA rate against 64 for 256 x 256 tiles
     // (bulk copies sustain ~65 per SM), at the price of a single TMEM accumulator
@@ -364,6 +365,17 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     pl->workspace_bytes = ws;
     pl->launches = (pl->prep_a != SGEMM_PREP_NONE) + (pl->prep_b != SGEMM_PREP_NONE) + 1 + (split > 1) +
                    (pl->sk_ctas > 0);
+
+    // FFMA products whose 128-wide tiles would run stream-K (under a wave of 304
+    // CTA slots) run 128 x 64 tiles at three CTAs per SM instead (456 slots; stream-K
+    // again, or a wave plus a last-wave split), which overlap the CTAs' prologues,
+    // segment switches and epilogues better.  Measured (L2 flushed): 2048^3 0.3185 ->
+    // 0.3065 ms, 1000 x 1300 x 4000 0.2208 -> 0.2075, 1100 x 700 x 6000 0.2024 ->
+    // 0.1881, 1500 x 1300 x 6000 0.458 -> 0.445, 2048^2 x 4096 0.606 -> 0.587,
+    // 1700^2 x 2048 0.2505 -> 0.2423; 1024^2 x 8192 even; 1250 x 1650 x 5000 0.3954
+    // -> 0.4031.
+    if (!tc && ffma_bn == 0 && pl->bn == 128 && pl->sk_ctas > 0 && g_force_bn.load() == 0)
+        make_plan(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, mode, num_sms, pl, allow_tail, 64);
 }
 
 // ---- devices ------------------------------------------------------------------------

@@ -263,23 +263,29 @@ def test_last_wave_split_ffma(mnk):
     assert H.padding_intact(p, out1, C)
 
 
-@pytest.mark.parametrize("mnk,ldc_pad,beta", [((2048, 2048, 2048), 3, 0.5), ((1000, 1300, 4000), 0, -1.0),
-                                               ((1024, 1024, 8192), 4, 0.0), ((12000, 50, 5200), 1, 1.5),
-                                               ((1100, 700, 6000), 2, 0.25), ((1250, 1650, 5000), 0, 0.0)])
-def test_ffma_stream_k(mnk, ldc_pad, beta):
+@pytest.mark.parametrize("mnk,ldc_pad,beta,bn", [((2048, 2048, 2048), 3, 0.5, 128), ((1000, 1300, 4000), 0, -1.0, 0),
+                                                  ((1024, 1024, 8192), 4, 0.0, 128), ((12000, 50, 5200), 1, 1.5, 0),
+                                                  ((1100, 700, 6000), 2, 0.25, 0), ((1250, 1650, 5000), 0, 0.0, 128)])
+def test_ffma_stream_k(mnk, ldc_pad, beta, bn):
     """FFMA products whose tiles fill less than one wave of CTA slots run stream-K:
     every CTA takes an equal range of (tile, k-block) iterations across tile
-    boundaries and a fix-up adds each tile's partial blocks in k order.  128- and
-    64-wide tiles, ragged edges, 2 to 6 segments per tile, beta 0 and not: the
-    oracle within 1e-5 and bitwise repeatable."""
+    boundaries and a fix-up adds each tile's partial blocks in k order.  The
+    planner's 64-wide tiles (three CTAs per SM) and, forced, the 128-wide ones;
+    ragged edges, 2 to 6 segments per tile, beta 0 and not: the oracle within
+    1e-5 and bitwise repeatable."""
     m, n, k = mnk
     p = synth.Problem(m, n, k, ldc=m + ldc_pad, alpha=0.75, beta=beta, dist="normal", seed=101)
-    plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "ffma")
-    preps = (plan["prep_a_name"] != "none") + (plan["prep_b_name"] != "none")
-    assert plan["sk_ctas"] > 0 and plan["launches"] == 2 + preps, plan
     A, B, C = synth.make(p)
-    out1, ok1 = H.run_gpu(p, "ffma", A, B, C)
-    out2, ok2 = H.run_gpu(p, "ffma", A, B, C)
+    try:
+        pg.force_plan(bn, 0)
+        plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "ffma")
+        preps = (plan["prep_a_name"] != "none") + (plan["prep_b_name"] != "none")
+        assert plan["sk_ctas"] > 0 and plan["launches"] == 2 + preps, plan
+        assert plan["bn"] == (bn or 64), plan
+        out1, ok1 = H.run_gpu(p, "ffma", A, B, C)
+        out2, ok2 = H.run_gpu(p, "ffma", A, B, C)
+    finally:
+        pg.force_plan(0, 0)
     assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
     if m * n <= 2 ** 21:
         cref, den = H.reference_full(p, A, B, C)

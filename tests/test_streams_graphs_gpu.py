@@ -149,7 +149,7 @@ def test_captured_last_wave_split_replays(mode):
     assert pg.device_status() == 0
 
 
-@pytest.mark.parametrize("mode,mnk,trans", [("ffma", (2048, 2048, 2048), "NN"), ("ffma", (1500, 1300, 6000), "TT"),
+@pytest.mark.parametrize("mode,mnk,trans", [("ffma", (1000, 1300, 4000), "NN"), ("ffma", (1500, 1300, 6000), "TT"),
                                             ("3xtf32", (4096, 128, 8192), "NN"), ("3xtf32", (120, 5000, 9000), "TN")])
 def test_stream_k_captured_and_replayed(mode, mnk, trans):
     """Stream-K calls (FFMA, and 3xTF32 on single SMs; with transposed operands the
