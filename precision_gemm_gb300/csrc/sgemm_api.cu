@@ -221,6 +221,31 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // than two 128 x 128 ones: 16384^2 x 64 0.654 -> 0.611 ms, 16384^2 x 32 0.422 ->
     // 0.345, 8192^2 x 64 0.169 -> 0.158 (K = 128 1 % slower, K = 256 even).
     if (!tc && k <= 2 * kFfmaBK) bn = 64;
+    // FFMA over several waves: 128 x 128 tiles (two CTAs per SM) and 128 x 64 tiles
+    // (three) reach the same throughput within a wave, so the tile whose grid fills
+    // its waves better wins; the estimate counts a last wave at most half full as
+    // 1/s of a wave when it is split s ways along K.  Only with K >= 2048, where
+    // the split slices stay long (the ragged 3000 x 1500 x 777 problem ran 15 %
+    // slower on 128 x 64 tiles).  Measured (L2 flushed): 4096^3 0.962 -> 0.998 of
+    // the waves filled, 2.250 -> 2.174 ms; 6144^3 7.61 -> 7.25; 4096^2 x 2048 1.140
+    // -> 1.099; 8192^3 0.998 either way, 17.16 ms either way (keeps 128).
+    if (!tc && bn == 128 && ffma_bn == 0 && k >= 2048) {
+        const int64_t kb = cdiv(k, kFfmaBK);
+        auto filled = [&](int64_t tiles, int64_t cap) {
+            const int64_t full = tiles / cap, rem = tiles % cap;
+            double waves = static_cast<double>(full) + (rem > 0 ? 1.0 : 0.0);
+            if (rem > 0 && full >= 1 && 2 * rem <= cap && allow_tail) {
+                const int64_t sp = std::min<int64_t>({cap / rem, 4, kb / 8});
+                if (sp >= 2) waves = static_cast<double>(full) + 1.0 / static_cast<double>(sp);
+            }
+            return static_cast<double>(tiles) / (static_cast<double>(cap) * waves);
+        };
+        const int64_t sms = std::max(num_sms, 1);
+        const int64_t t128 = cdiv(m, kBM) * cdiv(n, 128);
+        if (t128 >= sms * ffma_ctas_per_sm(128) &&
+            filled(tiles64, sms * ffma_ctas_per_sm(64)) > filled(t128, sms * ffma_ctas_per_sm(128)) + 0.01)
+            bn = 64;
+    }
     if (ffma_bn) bn = ffma_bn;  // the re-plan below
     // TF32 on SM pairs: 256 x 512 tiles (two N = 256 MMAs per k-step) need 48 B/clk
     // per SM of operand feed at the full MMA rate against 64 for 256 x 256 tiles
