@@ -59,7 +59,7 @@ namespace {
 #define PG_FFMA_SK_FILL 90
 #endif
 #ifndef PG_FFMA_SK_MIN_KB
-#define PG_FFMA_SK_MIN_KB 32  // k-blocks per CTA at least
+#define PG_FFMA_SK_MIN_KB 4  // k-blocks per CTA at least
 #endif
 constexpr int kSkMaxSegsPerCta = 8;  // the kernels' segment tables
 // 3xTF32 stream-K on the single-SM tensor-core kernel (a compile-time switch),
@@ -337,11 +337,13 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
 
     // FFMA stream-K: when the tiles (times their K slices) leave more than a
     // tenth of the wave's CTA slots idle, every slot takes an equal share of all
-    // (tile, k-block) iterations instead -- at least 32 k-blocks each, so that the
-    // partial blocks' round trip and the fix-up launch are repaid (measured:
-    // 2048^3 0.341 -> 0.324 ms and 8192 x 64 x 8192 0.191 -> 0.169 at 54 per CTA;
-    // 1024^3 at 7 and 1000 x 1300 x 1500 at 14 per CTA were slower than the K
-    // split).
+    // (tile, k-block) iterations instead -- at least 4 k-blocks each (measured:
+    // 2048^3 0.341 -> 0.324 ms and 8192 x 64 x 8192 0.191 -> 0.169 at 54 per CTA).
+    // The minimum was 32 while the fix-up was an ordinary launch and the tiles
+    // 128 wide (1024^3 at 7 and 1000 x 1300 x 1500 at 14 per CTA were slower than
+    // the K split then); with the fix-up dependent-launched and 128 x 64 tiles at
+    // three CTAs per SM, 4 measured best: row-major 1024^3 0.0549 -> 0.0532 ms,
+    // 1024^2 x 2048 0.0948 -> 0.0908, 1000 x 1300 x 1500 0.0948 -> 0.0903.
     if (PG_FFMA_SK && !tc && (bn == 64 || bn == 128) && fs == 0 && allow_tail && tiles < capacity &&
         100 * tiles * split < PG_FFMA_SK_FILL * capacity && tiles * pl->k_blocks >= PG_FFMA_SK_MIN_KB * capacity &&
         sk_segs_per_cta(tiles, pl->k_blocks, capacity) <= kSkMaxSegsPerCta) {

@@ -81,14 +81,16 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
         assert tiles >= capacity, where
     else:
         assert p["tail_split"] == 1, where
-    # FFMA stream-K: only where the tiles (with their K slices) leave over a tenth of
-    # one wave's CTA slots idle and every slot gets at least 32 k-blocks; all slots run
+    # stream-K: only where the tiles (with their K slices) leave over a tenth of one
+    # wave's CTA slots idle and every slot gets at least 4 (FFMA) or 32 (3xTF32)
+    # k-blocks; all slots run
     if p["sk_ctas"] > 0:  # FFMA, or 3xTF32 on single SMs
         tiles = p["tiles_m"] * p["tiles_n"]
         capacity = sms * p["ctas_per_sm"]
         assert (name == "ffma" and p["bn"] in (64, 128)) or (name == "tc" and mode == "3xtf32" and p["bn"] == 128), where
         assert s == 1 and p["tail_split"] == 1, where
-        assert p["sk_ctas"] == capacity and tiles < capacity and tiles * p["k_blocks"] >= 32 * capacity, where
+        min_kb = 4 if name == "ffma" else 32
+        assert p["sk_ctas"] == capacity and tiles < capacity and tiles * p["k_blocks"] >= min_kb * capacity, where
     # launch resources fit one SM
     assert 0 < p["smem_bytes"] <= SMEM_PER_CTA, where
     assert p["ctas_per_sm"] * p["smem_bytes"] <= SMEM_PER_SM, where
