@@ -58,6 +58,14 @@ namespace {
 #ifndef PG_FFMA_SK_FILL
 #define PG_FFMA_SK_FILL 90
 #endif
+// K slices of a last-wave tile at most: FFMA (measured, 128 x 64 tiles at 2048^2 x
+// 4096: 0.587 -> 0.574 ms with 8 against 4) and SM pairs
+#ifndef PG_TAIL_MAX_SPLIT
+#define PG_TAIL_MAX_SPLIT 8
+#endif
+#ifndef PG_TAIL_MAX_SPLIT_PAIRS
+#define PG_TAIL_MAX_SPLIT_PAIRS 4
+#endif
 #ifndef PG_FFMA_SK_MIN_KB
 #define PG_FFMA_SK_MIN_KB 4  // k-blocks per CTA at least
 #endif
@@ -369,12 +377,13 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
 
     // Last-wave split (SM pairs, and FFMA): when the tiles fill whole waves and a
     // last wave at most half full, cut each last-wave tile's K into s slices (at
-    // least 8 K blocks each, s <= 4) so the last wave keeps every pair (every
-    // FFMA CTA slot) busy.
+    // least 8 K blocks each; s <= 4 on SM pairs, <= 8 for FFMA) so the last wave
+    // keeps every pair (every FFMA CTA slot) busy.
     if ((pair || !tc) && split == 1 && pl->sk_ctas == 0 && g_force_split.load() == 0 && allow_tail) {
         const int64_t waves = tiles / capacity, rem = tiles % capacity;
         if (waves >= 1 && rem > 0 && 2 * rem <= capacity) {
-            const int64_t s = std::min<int64_t>({capacity / rem, 4, pl->k_blocks / 8});
+            const int64_t s = std::min<int64_t>(
+                {capacity / rem, pair ? PG_TAIL_MAX_SPLIT_PAIRS : PG_TAIL_MAX_SPLIT, pl->k_blocks / 8});
             if (s >= 2) {
                 pl->tail_tiles = static_cast<int>(rem);
                 pl->tail_split = static_cast<int>(s);

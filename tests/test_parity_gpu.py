@@ -244,11 +244,11 @@ def test_single_sm_3xtf32_presplit_b(mnk, tb, ld_pad, beta):
     assert H.padding_intact(p, out1, C)
 
 
-@pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4100, 2500, 600)])
+@pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4100, 2500, 600), (2048, 2048, 2048)])
 def test_last_wave_split_ffma(mnk):
-    """FFMA: the last partial wave's 128x128 tiles run as 2-4 K slices; the warp of the
-    last slice to finish sums the partial blocks in slice order -- ragged edges, beta != 0,
-    bitwise repeatable."""
+    """FFMA: the last partial wave's tiles run as 2-8 K slices (2048^3: 128 x 64 tiles,
+    eight slices); the warp of the last slice to finish sums the partial blocks in
+    slice order -- ragged edges, beta != 0, bitwise repeatable."""
     m, n, k = mnk
     p = synth.Problem(m, n, k, ldc=m + 3, alpha=-1.25, beta=0.5, dist="normal", seed=47)
     plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "ffma")

@@ -71,10 +71,11 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
     s, per = p["split_k"], p["k_blocks_per_split"]
     assert 1 <= s <= p["k_blocks"], where
     assert s * per >= p["k_blocks"] and (s - 1) * per < p["k_blocks"], where
-    # last-wave split: only without split-K, on the kernels that have it, 2..4 slices of >= 8 K blocks
+    # last-wave split: only without split-K, on the kernels that have it, 2..4 (SM pairs) or 2..8 (FFMA)
+    # slices of >= 8 K blocks
     if p["tail_split"] > 1:
         assert s == 1 and name in ("tc2", "ffma"), where
-        assert 2 <= p["tail_split"] <= 4 and p["tail_split"] * 8 <= p["k_blocks"], where
+        assert 2 <= p["tail_split"] <= (4 if name == "tc2" else 8) and p["tail_split"] * 8 <= p["k_blocks"], where
         tiles = p["tiles_m"] * p["tiles_n"]
         capacity = max(sms // 2, 1) if name == "tc2" else sms * p["ctas_per_sm"]
         assert p["tail_tiles"] == tiles % capacity and 2 * p["tail_tiles"] <= capacity, where
