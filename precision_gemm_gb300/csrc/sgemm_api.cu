@@ -243,7 +243,7 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
             const int64_t full = tiles / cap, rem = tiles % cap;
             double waves = static_cast<double>(full) + (rem > 0 ? 1.0 : 0.0);
             if (rem > 0 && full >= 1 && 2 * rem <= cap && allow_tail) {
-                const int64_t sp = std::min<int64_t>({cap / rem, 4, kb / 8});
+                const int64_t sp = std::min<int64_t>({cap / rem, PG_TAIL_MAX_SPLIT, kb / 8});
                 if (sp >= 2) waves = static_cast<double>(full) + 1.0 / static_cast<double>(sp);
             }
             return static_cast<double>(tiles) / (static_cast<double>(cap) * waves);

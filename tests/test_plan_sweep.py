@@ -174,3 +174,48 @@ def test_plan_trivial_shapes_launch_nothing_or_scale(lib):
                               max(m, 1), mode)
             assert p["kernel_name"] == kernel and p["launches"] == launches, (mode, m, n, k, alpha, beta)
             assert p["workspace_bytes"] == 0
+
+
+def _filled(tiles, cap, kb):
+    """Share of a grid's CTA-slot waves that its tiles fill, a last wave at most half
+    full and split s ways along K (s >= 2) counting as 1/s of a wave."""
+    full, rem = divmod(tiles, cap)
+    waves = full + (1 if rem else 0)
+    if rem and full >= 1 and 2 * rem <= cap:
+        s = min(cap // rem, 8, kb // 8)
+        if s >= 2:
+            waves = full + 1.0 / s
+    return tiles / (cap * waves)
+
+
+@pytest.mark.parametrize("sms", [152, 132, 80])
+def test_ffma_tile_width_rules(lib, sms):
+    """The FFMA planner's width choices, for n > 64: 128 x 64 tiles (three CTAs per
+    SM) when K <= 64; for tiny products (under 2 GFLOP, 128 x 64 tiles filling at
+    most half the SMs); when the 128-wide tiles would run stream-K; and, over
+    several waves with K >= 2048, when their grid fills its waves better by more
+    than 0.01.  Otherwise 128 x 128 (two CTAs per SM)."""
+    rng = np.random.default_rng(2027 + sms)
+    shapes = [(4096, 4096, 4096), (8192, 8192, 8192), (6144, 6144, 6144), (2048, 2048, 2048), (1000, 1300, 4000),
+              (16384, 16384, 64), (16384, 16384, 65), (3000, 1500, 777)]
+    shapes += [(int(rng.integers(200, 9000)), int(rng.integers(65, 9000)), int(rng.choice([32, 64, 500, 2048, 5000])))
+               for _ in range(120)]
+    for m, n, k in shapes:
+        p = pg.sgemm_plan("N", "N", m, n, k, 1.0, 256, m, 256, k, 0.0, 256, m, "ffma", num_sms=sms)
+        where = (m, n, k, sms, p["bn"])
+        assert p["bn"] in (64, 128), where
+        assert p["ctas_per_sm"] == (3 if p["bn"] == 64 else 2), where
+        if k <= 64:
+            assert p["bn"] == 64, where
+            continue
+        pg.force_plan(128, 0)
+        try:
+            p128 = pg.sgemm_plan("N", "N", m, n, k, 1.0, 256, m, 256, k, 0.0, 256, m, "ffma", num_sms=sms)
+        finally:
+            pg.force_plan(0, 0)
+        kb = _cdiv(k, 32)
+        t128, t64 = _cdiv(m, 128) * _cdiv(n, 128), _cdiv(m, 128) * _cdiv(n, 64)
+        wave_rule = k >= 2048 and t128 >= 2 * sms and _filled(t64, 3 * sms, kb) > _filled(t128, 2 * sms, kb) + 0.01
+        tiny = 2 * t64 <= sms and 2.0 * m * n * k <= 2e9
+        want64 = tiny or p128["sk_ctas"] > 0 or wave_rule
+        assert (p["bn"] == 64) == want64, (where, p128["sk_ctas"], wave_rule)
