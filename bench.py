@@ -352,10 +352,11 @@ def run_ours(args, wl_name):
 
     # Dominant kernel: the mode whose launches take longest in the step.
     dom = max(modes, key=lambda m: mode_info[m]["ms_median"])
-    kname = pg.sgemm_plan(p.transa, p.transb, p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc,
-                          dom, num_sms)["kernel_name"]
-    dom_kernel = "%s_gemm_kernel%s" % (kname, "" if dom == "ffma" else " (%s)" % dom)
-    traffic = read_traffic(dom, kname, wl_name)
+    dplan = pg.sgemm_plan(p.transa, p.transb, p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc,
+                          dom, num_sms)
+    kname, tile = dplan["kernel_name"], "%dx%d" % (dplan["bm"], dplan["bn"])
+    dom_kernel = "%s_gemm_kernel (%s%s tiles)" % (kname, "" if dom == "ffma" else dom + ", ", tile)
+    traffic = read_traffic(dom, kname, tile, wl_name)
     if dom == "ffma":
         roofline = {"bound": "alu", "achieved": mode_info[dom]["tflops"], "peak": fp32_peak, "unit": "TFLOP/s",
                     "frac": mode_info[dom]["tflops"] / fp32_peak,
@@ -455,11 +456,11 @@ def run_sweep(args, modes, pk, stream):
     return out
 
 
-def read_traffic(mode: str, kname: str, wl_name: str):
+def read_traffic(mode: str, kname: str, tile: str, wl_name: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary
-    (profiles/<mode>_<workload>.md: 'traffic_bytes_per_launch: N' plus the hash of
-    the kernel source it was taken on); None when absent or taken on a different
-    source."""
+    (profiles/<mode>_<workload>.md: 'traffic_bytes_per_launch: N' plus the tile shape
+    and the hash of the kernel source it was taken on); None when absent, or taken
+    on a different source or tile shape."""
     import hashlib
     src = "%s_kernel.cu" % kname
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (mode, wl_name))
@@ -469,7 +470,7 @@ def read_traffic(mode: str, kname: str, wl_name: str):
         return None
     digest = hashlib.sha256(open(os.path.join(ROOT, "precision_gemm_gb300", "csrc", src), "rb").read()).hexdigest()
     fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line and not line.startswith("#"))
-    if fields.get("source_sha256", "").strip() != digest:
+    if fields.get("source_sha256", "").strip() != digest or fields.get("tile", "").strip() != tile:
         return None
     try:
         return int(fields["traffic_bytes_per_launch"].strip())

@@ -231,8 +231,8 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     if (!tc && k <= 2 * kFfmaBK) bn = 64;
     // FFMA over several waves: 128 x 128 tiles (two CTAs per SM) and 128 x 64 tiles
     // (three) reach the same throughput within a wave, so the tile whose grid fills
-    // its waves better wins; the estimate counts a last wave at most half full as
-    // 1/s of a wave when it is split s ways along K.  Only with K >= 2048, where
+    // its waves better wins (the 128 x 64 one on a tie); the estimate counts a last
+    // wave at most half full as 1/s of a wave when it is split s ways along K.  Only with K >= 2048, where
     // the split slices stay long (the ragged 3000 x 1500 x 777 problem ran 15 %
     // slower on 128 x 64 tiles).  Measured (L2 flushed): 4096^3 0.962 -> 0.998 of
     // the waves filled, 2.250 -> 2.174 ms; 6144^3 7.61 -> 7.25; 4096^2 x 2048 1.140
@@ -250,8 +250,16 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
         };
         const int64_t sms = std::max(num_sms, 1);
         const int64_t t128 = cdiv(m, kBM) * cdiv(n, 128);
-        if (t128 >= sms * ffma_ctas_per_sm(128) &&
-            filled(tiles64, sms * ffma_ctas_per_sm(64)) > filled(t128, sms * ffma_ctas_per_sm(128)) + 0.01)
+// On a tie (within 0.01) the 128 x 64 tile: it also runs spill-free (158
+// registers at three CTAs per SM against 48 B of spills at the 128-register cap
+// of the 128 x 128 tile) and measured a little faster: 8192^3 17.168 -> 17.132
+// ms, 16384^3 137.02 -> 136.64, 8192^2 x 2048 4.345 -> 4.318 (beta = 1).
+#ifndef PG_FFMA_PREFER64
+#define PG_FFMA_PREFER64 1
+#endif
+        const double f64 = filled(tiles64, sms * ffma_ctas_per_sm(64));
+        const double f128 = filled(t128, sms * ffma_ctas_per_sm(128));
+        if (t128 >= sms * ffma_ctas_per_sm(128) && (PG_FFMA_PREFER64 ? f64 >= f128 - 0.01 : f64 > f128 + 0.01))
             bn = 64;
     }
     if (ffma_bn) bn = ffma_bn;  // the re-plan below

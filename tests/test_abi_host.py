@@ -120,13 +120,14 @@ def plan(m, n, k, mode="ffma", transa="N", transb="N", lda=None, ldb=None, ldc=N
 def test_plan_square_uses_wide_tiles_and_no_split(lib):
     for mode in ("ffma", "tf32", "3xtf32"):
         p = plan(8192, 8192, 8192, mode)
-        # FFMA: 128 x 128 tiles, two CTAs per SM; tensor cores on SM pairs: 256 x 512 tiles
-        # for TF32 (long K, two waves or more of tiles), 256 x 256 for 3xTF32
-        bm, bn = {"ffma": (128, 128), "tf32": (256, 512), "3xtf32": (256, 256)}[mode]
+        # FFMA: 128 x 64 tiles, three CTAs per SM (they fill their waves as well as 128 x 128
+        # tiles at two per SM, and win the tie); tensor cores on SM pairs: 256 x 512 tiles for
+        # TF32 (long K, two waves or more of tiles), 256 x 256 for 3xTF32
+        bm, bn = {"ffma": (128, 64), "tf32": (256, 512), "3xtf32": (256, 256)}[mode]
         assert p["bn"] == bn and p["bm"] == bm and p["split_k"] == 1
         assert p["tiles_m"] == 8192 // bm and p["tiles_n"] == 8192 // bn
         assert p["kernel_name"] == ("ffma" if mode == "ffma" else "tc2")
-        assert p["ctas_per_sm"] == (2 if mode == "ffma" else 1)
+        assert p["ctas_per_sm"] == (3 if mode == "ffma" else 1)
     assert plan(8192, 8192, 8192, "ffma")["prep_a_name"] == "none"
     # 3xTF32 on SM pairs: a split pre-pass per operand, then the GEMM
     x = plan(8192, 8192, 8192, "3xtf32")
@@ -181,12 +182,13 @@ def test_plan_last_wave_split(lib):
     assert plan(256 * 10, 256 * 12, 4096, "tf32")["tail_split"] == 1         # 120 tiles: 44 > 76/2
     assert plan(4096, 4096, 96, "tf32")["tail_split"] == 1                  # 3 K blocks
     assert plan(512, 512, 8192, "tf32")["tail_split"] == 1                  # split-K instead
-    # FFMA: 4096 tiles of 128x128 over 152 SMs x 2 CTA slots = 13 waves + 144 tiles;
-    # the 144 last-wave tiles run as 2 K slices (288 blocks), in the same launch
-    f = plan(8192, 8192, 8192, "ffma")
-    assert f["tail_tiles"] == 4096 - 13 * 304 and f["tail_split"] == 2 and f["launches"] == 1
-    assert f["workspace_bytes"] >= 144 * 2 * 128 * 128 * 4
-    assert plan(16384, 16384, 16384, "ffma")["tail_split"] == 1  # 272-tile last wave: over half full
+    # FFMA: 2048 tiles of 128x64 over 152 SMs x 3 CTA slots = 4 waves + 224 tiles;
+    # the 224 last-wave tiles run as 2 K slices (448 blocks), in the same launch
+    f = plan(4096, 4096, 4096, "ffma")
+    assert f["bn"] == 64 and f["launches"] == 1
+    assert f["tail_tiles"] == 2048 - 4 * 456 and f["tail_split"] == 2
+    assert f["workspace_bytes"] >= 224 * 2 * 128 * 64 * 4
+    assert plan(8192, 8192, 8192, "ffma")["tail_split"] == 1  # 440-tile last wave: over half full
 
 
 def test_plan_skinny_k_uses_deterministic_split(lib):
