@@ -38,15 +38,22 @@ __device__ int g_device_status;
 
 namespace {
 
-// Tile rows per rasterisation group (a compile-time tunable; 4, 8 and 16 measured
-// within noise of each other at 8192^3).
 // FFMA: whole-tile results with beta = 0 leave through TMA stores (1) or
 // through thread stores of whole columns (0).
 #ifndef PG_FFMA_TMA_STORE
 #define PG_FFMA_TMA_STORE 1
 #endif
+// Tile rows per rasterisation group (a compile-time tunable; 4, 8 and 16 measured
+// within noise of each other at 8192^3; 8 and 32 slower than 16 for the SM-pair
+// kernels: TF32 1.087 -> 1.096 / 1.098 ms).
 #ifndef PG_GROUP_M
 #define PG_GROUP_M 16
+#endif
+// The FFMA kernel's own group: at 8192^3 (128 x 64 tiles) groups of 8 tile rows
+// cut its DRAM reads from 5.00 to 4.08 GB a launch (2: 9.55, 4: 5.69) at the same
+// time (17.13 ms), and 4096^3, 6144^3 and 2048^3 run the same with any of them.
+#ifndef PG_FFMA_GROUP_M
+#define PG_FFMA_GROUP_M 8
 #endif
 
 // FFMA stream-K (a compile-time switch): products whose tiles fill less than
@@ -233,11 +240,15 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // (three) reach the same throughput within a wave, so the tile whose grid fills
     // its waves better wins (the 128 x 64 one on a tie); the estimate counts a last
     // wave at most half full as 1/s of a wave when it is split s ways along K.  Only with K >= 2048, where
-    // the split slices stay long (the ragged 3000 x 1500 x 777 problem ran 15 %
-    // slower on 128 x 64 tiles).  Measured (L2 flushed): 4096^3 0.962 -> 0.998 of
-    // the waves filled, 2.250 -> 2.174 ms; 6144^3 7.61 -> 7.25; 4096^2 x 2048 1.140
-    // -> 1.099; 8192^3 0.998 either way, 17.16 ms either way (keeps 128).
-    if (!tc && bn == 128 && ffma_bn == 0 && k >= 2048) {
+    // the split slices stay long, or with K >= 512 and two or more waves of 128 x 64
+    // tiles (the ragged 3000 x 1500 x 777 problem, 1.26 waves, ran 16 % slower on
+    // 128 x 64 tiles).  Measured (L2 flushed): 4096^3 0.962 -> 0.998 of the waves
+    // filled, 2.250 -> 2.174 ms; 6144^3 7.61 -> 7.25; 4096^2 x 2048 1.140 -> 1.099;
+    // 4096^2 x 1024 0.585 -> 0.563; 4096 x 8192 x 1536 1.682 -> 1.627; 8192^2 x 512
+    // 1.112 -> 1.092; ties: 8192^2 x 1024 2.179 -> 2.162, 16384^2 x 1024 even,
+    // 1024 x 15409 x 1903 1.045 -> 1.051.
+    const bool ffma_waves64 = k >= 2048 || (k >= 512 && tiles64 >= 2 * std::max(num_sms, 1) * ffma_ctas_per_sm(64));
+    if (!tc && bn == 128 && ffma_bn == 0 && ffma_waves64) {
         const int64_t kb = cdiv(k, kFfmaBK);
         auto filled = [&](int64_t tiles, int64_t cap) {
             const int64_t full = tiles / cap, rem = tiles % cap;
@@ -892,7 +903,7 @@ int run(char transa, char transb, int64_t m, int64_t n, int64_t k, float alpha, 
         gp.sk_P = reinterpret_cast<float*>(cursor);
         cursor += region(tiles * gp.sk_maxseg * pl.bm * pl.bn);
     }
-    gp.group_m = PG_GROUP_M;
+    gp.group_m = (pl.kernel == SGEMM_KERNEL_FFMA) ? PG_FFMA_GROUP_M : PG_GROUP_M;
     gp.c_vec = aligned16(C) && (ldc % 4 == 0);
     gp.debug_flags = g_debug.load();
     gp.timeout_ns = g_timeout_ns.load();
@@ -996,7 +1007,7 @@ int run_noalloc(char transa, char transb, int64_t m, int64_t n, int64_t k, float
     gp.tiles_n = pl.tiles_n;
     gp.kb_total = pl.k_blocks;
     gp.kb_per_split = pl.k_blocks_per_split;
-    gp.group_m = PG_GROUP_M;
+    gp.group_m = (pl.kernel == SGEMM_KERNEL_FFMA) ? PG_FFMA_GROUP_M : PG_GROUP_M;
     gp.c_vec = aligned16(C) && (ldc % 4 == 0);
     gp.debug_flags = g_debug.load();
     gp.timeout_ns = g_timeout_ns.load();

@@ -244,18 +244,25 @@ def test_single_sm_3xtf32_presplit_b(mnk, tb, ld_pad, beta):
     assert H.padding_intact(p, out1, C)
 
 
-@pytest.mark.parametrize("mnk", [(2500, 2000, 1000), (2560, 2048, 700), (4100, 2500, 600), (2048, 2048, 2048)])
-def test_last_wave_split_ffma(mnk):
+@pytest.mark.parametrize("mnk,bn", [((2500, 2000, 1000), 0), ((2560, 2048, 700), 0), ((4100, 2500, 600), 128),
+                                    ((2048, 2048, 2048), 0), ((4000, 4090, 1000), 0)])
+def test_last_wave_split_ffma(mnk, bn):
     """FFMA: the last partial wave's tiles run as 2-8 K slices (2048^3: 128 x 64 tiles,
     eight slices); the warp of the last slice to finish sums the partial blocks in
-    slice order -- ragged edges, beta != 0, bitwise repeatable."""
+    slice order -- ragged edges, beta != 0, bitwise repeatable.  128-wide tiles are
+    forced where the planner would take 64-wide ones."""
     m, n, k = mnk
     p = synth.Problem(m, n, k, ldc=m + 3, alpha=-1.25, beta=0.5, dist="normal", seed=47)
-    plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "ffma")
-    assert plan["kernel_name"] == "ffma" and plan["tail_split"] > 1, plan
     A, B, C = synth.make(p)
-    out1, ok1 = H.run_gpu(p, "ffma", A, B, C)
-    out2, ok2 = H.run_gpu(p, "ffma", A, B, C)
+    try:
+        pg.force_plan(bn, 0)
+        plan = pg.sgemm_plan("N", "N", m, n, k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, "ffma")
+        assert plan["kernel_name"] == "ffma" and plan["tail_split"] > 1, plan
+        assert bn == 0 or plan["bn"] == bn, plan
+        out1, ok1 = H.run_gpu(p, "ffma", A, B, C)
+        out2, ok2 = H.run_gpu(p, "ffma", A, B, C)
+    finally:
+        pg.force_plan(0, 0)
     assert ok1 and ok2 and torch.equal(out1.view(torch.int32), out2.view(torch.int32))
     cref, den = H.reference_full(p, A, B, C)
     res = oracle.check(H.logical(p, out1), cref, den, oracle.TOL["ffma"])

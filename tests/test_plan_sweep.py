@@ -193,12 +193,12 @@ def test_ffma_tile_width_rules(lib, sms):
     """The FFMA planner's width choices, for n > 64: 128 x 64 tiles (three CTAs per
     SM) when K <= 64; for tiny products (under 2 GFLOP, 128 x 64 tiles filling at
     most half the SMs); when the 128-wide tiles would run stream-K; and, over
-    several waves with K >= 2048, unless the 128 x 128 grid fills its waves better
-    by more than 0.01.  Otherwise 128 x 128 (two CTAs per SM)."""
+    several waves with K >= 2048 (or K >= 512 and two waves of 128 x 64 tiles),
+    unless the 128 x 128 grid fills its waves better by more than 0.01.  Otherwise 128 x 128 (two CTAs per SM)."""
     rng = np.random.default_rng(2027 + sms)
     shapes = [(4096, 4096, 4096), (8192, 8192, 8192), (6144, 6144, 6144), (2048, 2048, 2048), (1000, 1300, 4000),
               (16384, 16384, 64), (16384, 16384, 65), (3000, 1500, 777)]
-    shapes += [(int(rng.integers(200, 9000)), int(rng.integers(65, 9000)), int(rng.choice([32, 64, 500, 2048, 5000])))
+    shapes += [(int(rng.integers(200, 9000)), int(rng.integers(65, 9000)), int(rng.choice([32, 64, 500, 512, 1024, 2048, 5000])))
                for _ in range(120)]
     for m, n, k in shapes:
         p = pg.sgemm_plan("N", "N", m, n, k, 1.0, 256, m, 256, k, 0.0, 256, m, "ffma", num_sms=sms)
@@ -215,7 +215,8 @@ def test_ffma_tile_width_rules(lib, sms):
             pg.force_plan(0, 0)
         kb = _cdiv(k, 32)
         t128, t64 = _cdiv(m, 128) * _cdiv(n, 128), _cdiv(m, 128) * _cdiv(n, 64)
-        wave_rule = k >= 2048 and t128 >= 2 * sms and _filled(t64, 3 * sms, kb) >= _filled(t128, 2 * sms, kb) - 0.01
+        long_k = k >= 2048 or (k >= 512 and t64 >= 2 * 3 * sms)
+        wave_rule = long_k and t128 >= 2 * sms and _filled(t64, 3 * sms, kb) >= _filled(t128, 2 * sms, kb) - 0.01
         tiny = 2 * t64 <= sms and 2.0 * m * n * k <= 2e9
         want64 = tiny or p128["sk_ctas"] > 0 or wave_rule
         assert (p["bn"] == 64) == want64, (where, p128["sk_ctas"], wave_rule)
