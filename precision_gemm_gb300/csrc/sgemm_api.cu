@@ -277,12 +277,30 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // TF32 on SM pairs: 256 x 512 tiles (two N = 256 MMAs per k-step) need 48 B/clk
     // per SM of operand feed at the full MMA rate against 64 for 256 x 256 tiles
     // (bulk copies sustain ~65 per SM), at the price of a single TMEM accumulator
-    // (the epilogue of a tile no longer overlaps the next tile's MMAs).  Faster
-    // with K >= 4096 and at least two waves of tiles: 8192^3 897 -> 964 TFLOP/s,
-    // 6144^3 875 -> 936, 16384 x 4096 x 8192 889 -> 959; at K = 2048 1 % slower.
-    if (tc && !split3 && m > kBM && bn == 256 && k >= 4096 &&
-        cdiv(m, 2 * kBM) * cdiv(n, 512) >= 2 * std::max(num_sms / 2, 1))
-        bn = 512;
+    // (the epilogue of a tile no longer overlaps the next tile's MMAs).  With K >=
+    // 2048 a wave of 256 x 512 tiles takes about 1.8 times as long as a wave of
+    // 256 x 256 ones (half the tiles), so the wider tile wins when 1.8 x its waves
+    // (a partial last wave counted whole: it is not split, the split's 512-column
+    // partial blocks measured slower than a whole extra wave) is under the 256-wide
+    // grid's waves (a last wave at most half full split s ways counted as 1/s + 0.4,
+    // the 0.4 for the slices' partial blocks and their sum).  Measured (L2 flushed,
+    // ms, 256 -> 512): 4096^3 0.178 -> 0.160, 4096^2 x 2048 0.106 -> 0.089, 8192^2 x
+    // 2048 0.321 -> 0.302, 16384 x 4096 x 4096 0.611 -> 0.562, 3000 x 5000 x 4096
+    // 0.202 -> 0.163, 8192^3 1.17 -> 1.09; kept at 256: 3072 x 4096 x 4096 0.134
+    // (0.170 on 512), 4096 x 2560 x 4096 0.142 (0.179).
+    if (tc && !split3 && m > kBM && bn == 256 && k >= 2048) {
+        const int64_t pairs = std::max(num_sms / 2, 1);
+        const int64_t t512 = cdiv(m, 2 * kBM) * cdiv(n, 512), t256 = cdiv(m, 2 * kBM) * cdiv(n, 256);
+        if (t512 >= pairs) {
+            const int64_t full = t256 / pairs, rem = t256 % pairs;
+            double w256 = static_cast<double>(full) + (rem > 0 ? 1.0 : 0.0);
+            if (rem > 0 && full >= 1 && 2 * rem <= pairs && allow_tail) {
+                const int64_t sp = std::min<int64_t>({pairs / rem, PG_TAIL_MAX_SPLIT_PAIRS, cdiv(k, tc2_bk(false)) / 8});
+                if (sp >= 2) w256 = static_cast<double>(full) + 1.0 / static_cast<double>(sp) + 0.4;
+            }
+            if (1.8 * static_cast<double>(cdiv(t512, pairs)) < w256) bn = 512;
+        }
+    }
     const int fbn = g_force_bn.load();
     if (fbn) bn = (fbn == 512 && (!tc || split3 || m <= kBM)) ? 256 : fbn;  // 512: TF32 on SM pairs only
     pl->bn = bn;
@@ -398,7 +416,8 @@ void make_plan(char transa, char transb, int64_t m, int64_t n, int64_t k, float 
     // last wave at most half full, cut each last-wave tile's K into s slices (at
     // least 8 K blocks each; s <= 4 on SM pairs, <= 8 for FFMA) so the last wave
     // keeps every pair (every FFMA CTA slot) busy.
-    if ((pair || !tc) && split == 1 && pl->sk_ctas == 0 && g_force_split.load() == 0 && allow_tail) {
+    if ((pair || !tc) && split == 1 && pl->sk_ctas == 0 && g_force_split.load() == 0 && allow_tail &&
+        (pl->bn != 512 || fbn == 512)) {  // 256 x 512 tiles: only when forced (slower than a whole wave)
         const int64_t waves = tiles / capacity, rem = tiles % capacity;
         if (waves >= 1 && rem > 0 && 2 * rem <= capacity) {
             const int64_t s = std::min<int64_t>(

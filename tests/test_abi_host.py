@@ -153,8 +153,14 @@ def test_plan_square_uses_wide_tiles_and_no_split(lib):
 def test_plan_tf32_512_wide_pair_tiles(lib):
     assert plan(6144, 6144, 6144, "tf32")["bn"] == 512
     assert plan(16384, 4096, 8192, "tf32")["bn"] == 512
-    assert plan(8192, 8192, 2048, "tf32")["bn"] == 256       # K < 4096: the overlapped epilogue wins
-    assert plan(4096, 4096, 16384, "tf32")["bn"] == 256      # 128 tiles of 256 x 512: under two waves
+    assert plan(8192, 8192, 2048, "tf32")["bn"] == 512       # 7 waves against 13 + a split last wave
+    assert plan(4096, 4096, 16384, "tf32")["bn"] == 512      # 2 waves against 3 + a split last wave
+    assert plan(3072, 4096, 4096, "tf32")["bn"] == 256       # 2 waves of 96 tiles against 3 of 192
+    assert plan(4096, 2560, 4096, "tf32")["bn"] == 256       # 2 waves (80 tiles) against 2 + a split
+    assert plan(2048, 2048, 8192, "tf32")["bn"] == 256       # 32 tiles of 256 x 512: under one wave
+    assert plan(4096, 4096, 2048, "tf32")["bn"] == 512
+    assert plan(8192, 8192, 1024, "tf32")["bn"] == 256       # K < 2048
+    assert plan(8192, 8192, 8192, "tf32")["tail_split"] == 1  # 256 x 512 tiles do not split a last wave
     assert plan(8192, 8192, 8192, "3xtf32")["bn"] == 256     # 3xTF32 keeps 256 x 256
     assert plan(16384, 16384, 64, "tf32")["bn"] == 256       # skinny K
     # forcing 512 where it does not exist means 256
@@ -169,11 +175,11 @@ def test_plan_tf32_512_wide_pair_tiles(lib):
 
 
 def test_plan_last_wave_split(lib):
-    # SM pairs: 256 tiles of 256x256 over 76 pairs = 3 full waves + 28 tiles; the last
-    # wave's 28 tiles run as 2 K slices each (56 units keep the pairs busy)
-    p = plan(4096, 4096, 4096, "tf32")
-    assert p["tail_tiles"] == 28 and p["tail_split"] == 2 and p["split_k"] == 1
-    assert p["workspace_bytes"] >= 28 * 2 * 256 * 256 * 4
+    # SM pairs: 160 tiles of 256x256 over 76 pairs = 2 full waves + 8 tiles; the last
+    # wave's 8 tiles run as 4 K slices each (32 units)
+    p = plan(4096, 2560, 4096, "tf32")
+    assert p["bn"] == 256 and p["tail_tiles"] == 8 and p["tail_split"] == 4 and p["split_k"] == 1
+    assert p["workspace_bytes"] >= 8 * 4 * 256 * 256 * 4
     q = plan(8192, 8192, 8192, "3xtf32")
     assert q["tail_tiles"] == 1024 - 13 * 76 and q["tail_split"] == 2
     # no split when the tiles fill whole waves, the last wave is over half full,

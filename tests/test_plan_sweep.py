@@ -64,6 +64,7 @@ def _check(p, m, n, k, mode, transa, transb, lda, ldb, aligned, sms):
     assert p["bn"] in (64, 128, 256, 512), where
     if p["bn"] == 512:
         assert mode == "tf32" and name == "tc2", where
+        assert p["tail_split"] == 1, where  # a 256 x 512 tile's last wave is never split
     # the tiles and the K blocks cover the product exactly
     assert p["tiles_m"] == _cdiv(m, p["bm"]) and p["tiles_n"] == _cdiv(n, p["bn"]), where
     assert p["k_blocks"] == _cdiv(k, p["bk"]), where
@@ -220,3 +221,34 @@ def test_ffma_tile_width_rules(lib, sms):
         tiny = 2 * t64 <= sms and 2.0 * m * n * k <= 2e9
         want64 = tiny or p128["sk_ctas"] > 0 or wave_rule
         assert (p["bn"] == 64) == want64, (where, p128["sk_ctas"], wave_rule)
+
+
+@pytest.mark.parametrize("sms", [152, 132, 80])
+def test_tf32_pair_tile_width_rule(lib, sms):
+    """TF32 on SM pairs with K >= 2048: 256 x 512 tiles when they make at least one
+    wave of pairs and 1.8 x their waves (a partial last wave counted whole) is under
+    the 256 x 256 grid's waves, a last wave at most half full split s ways counting
+    1/s + 0.4; otherwise 256 x 256.  Shorter K keeps 256 x 256."""
+    rng = np.random.default_rng(3031 + sms)
+    shapes = [(4096, 4096, 4096), (3072, 4096, 4096), (4096, 2560, 4096), (8192, 8192, 2048), (8192, 8192, 1024),
+              (3000, 5000, 4096), (2048, 2048, 8192), (16384, 4096, 8192)]
+    shapes += [(int(rng.integers(300, 12000)), int(rng.integers(300, 12000)), int(rng.choice([1024, 2048, 3000, 8192])))
+               for _ in range(150)]
+    pairs = max(sms // 2, 1)
+    for m, n, k in shapes:
+        p = pg.sgemm_plan("N", "N", m, n, k, 1.0, 256, m, 256, k, 0.0, 256, m, "tf32", num_sms=sms)
+        if p["kernel_name"] != "tc2":
+            continue
+        where = (m, n, k, sms, p["bn"])
+        t512, t256 = _cdiv(m, 256) * _cdiv(n, 512), _cdiv(m, 256) * _cdiv(n, 256)
+        full, rem = divmod(t256, pairs)
+        w256 = full + (1 if rem else 0)
+        if rem and full >= 1 and 2 * rem <= pairs:
+            sp = min(pairs // rem, 4, _cdiv(k, 32) // 8)
+            if sp >= 2:
+                w256 = full + 1.0 / sp + 0.4
+        want512 = k >= 2048 and t512 >= pairs and 1.8 * _cdiv(t512, pairs) < w256
+        if n > 256 and p["split_k"] == 1:
+            assert (p["bn"] == 512) == want512, where
+        else:
+            assert p["bn"] != 512, where
