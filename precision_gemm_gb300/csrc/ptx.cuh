@@ -145,16 +145,21 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
 // split_tf32 on every input, in fewer instructions per value.
 template <int N>
 __device__ __forceinline__ void split_tf32_batch(const float (&x)[N], uint32_t (&big)[N], uint32_t (&small)[N]) {
-    uint32_t emax = 0;
+    // The rare inputs are NaN and magnitudes from 0x7F7FF000 up (infinities, and
+    // finite values that round to the all-ones exponent): one NaN-propagating
+    // maximum of the magnitudes per value finds them (one instruction where
+    // tracking the exponents of x and big took two; 8192 x 64 x 8192 3xTF32
+    // 0.0774 -> 0.0748 ms).
+    float vmax = 0.0f;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
         const uint32_t u = __float_as_uint(x[k]);
         const uint32_t b = (u + 0x1000u) & 0xFFFFE000u;
         big[k] = b;
         small[k] = __float_as_uint(x[k] - __uint_as_float(b));
-        emax = max(emax, (u | b) & 0x7F800000u);
+        asm("max.NaN.xorsign.abs.f32 %0, %0, %1;" : "+f"(vmax) : "f"(x[k]));
     }
-    if (emax == 0x7F800000u) {
+    if (!(fabsf(vmax) < __uint_as_float(0x7F7FF000u))) {
 #pragma unroll
         for (int k = 0; k < N; ++k) {
             float bf, sf;
