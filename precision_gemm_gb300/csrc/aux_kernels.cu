@@ -87,8 +87,12 @@ template <bool SPLIT>
 __global__ void __launch_bounds__(256, SPLIT ? 3 : 4)
     prep_copy_kernel(const float* __restrict__ src, int64_t lds, int64_t rows, int64_t cols,
                      float* __restrict__ dst, float* __restrict__ dst_small, int64_t ldd, int tx_shift,
-                     int by_rows) {
-    pdl_wait();  // launched after the other operand's pass: that pass's completion
+                     int by_rows, int wait_last) {
+    // Launched after the other operand's pass (independent data): with wait_last
+    // the two passes overlap and this one waits for the other only before it
+    // retires, so that the GEMM, which waits for this pass, also finds the other
+    // one complete.
+    if (!wait_last) pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();  // the GEMM may be scheduled; it waits for this pass
     const Sweep w = sweep_setup(tx_shift);
     float x[kU];
@@ -104,6 +108,7 @@ __global__ void __launch_bounds__(256, SPLIT ? 3 : 4)
                 dst[c * ldd + r] = x[u];
             }
         });
+    if (wait_last) pdl_wait();
 }
 
 // prep_copy_kernel for a 16-byte aligned src with lds % 4 == 0 (dst is 256-byte
@@ -115,8 +120,9 @@ __global__ void __launch_bounds__(256, SPLIT ? 3 : 4)
 template <bool SPLIT>
 __global__ void __launch_bounds__(256) prep_copy_vec_kernel(const float* __restrict__ src, int64_t lds, int64_t rows,
                                                             int64_t cols, float* __restrict__ dst,
-                                                            float* __restrict__ dst_small, int64_t ldd) {
-    pdl_wait();
+                                                            float* __restrict__ dst_small, int64_t ldd,
+                                                            int wait_last) {
+    if (!wait_last) pdl_wait();  // as in prep_copy_kernel
     if (threadIdx.x == 0) pdl_trigger();
     const int64_t rq = (rows + 3) / 4;  // chunks per column
     const int64_t total = rq * cols;
@@ -165,6 +171,7 @@ __global__ void __launch_bounds__(256) prep_copy_vec_kernel(const float* __restr
             }
         }
     }
+    if (wait_last) pdl_wait();
 }
 
 // dst(r, c) = src(c, r): 32 x 32 tiles through shared memory so that both the
@@ -173,10 +180,11 @@ template <bool SPLIT>
 __global__ void __launch_bounds__(256) prep_transpose_kernel(const float* __restrict__ src, int64_t lds,
                                                              int64_t rows, int64_t cols,
                                                              float* __restrict__ dst,
-                                                             float* __restrict__ dst_small, int64_t ldd) {
+                                                             float* __restrict__ dst_small, int64_t ldd,
+                                                             int wait_last) {
     __shared__ float tile[32][33];
-    pdl_wait();
-    if (threadIdx.x == 0) pdl_trigger();
+    if (!wait_last) pdl_wait();  // as in prep_copy_kernel
+    if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
     const int64_t tiles_r = (rows + 31) / 32;
     const int64_t tiles_c = (cols + 31) / 32;
     for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
@@ -204,6 +212,7 @@ __global__ void __launch_bounds__(256) prep_transpose_kernel(const float* __rest
         }
         __syncthreads();
     }
+    if (wait_last) pdl_wait();
 }
 
 // Loads of the split-K reductions run up to kS slices ahead of the additions.
@@ -468,6 +477,7 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
                         float* dst_small, int64_t ldd, int num_sms, cudaStream_t stream, bool after_previous) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
     const bool dep = PG_PDL_PREP && after_previous;
+    const int wl = (dep && PG_PREP_OVERLAP) ? 1 : 0;
     if (transposed) {
         const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
         int64_t g = static_cast<int64_t>(num_sms) * 8;
@@ -475,9 +485,9 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
         const dim3 block(32, 8);
         if (dst_small)
             return launch_kernel(dep, prep_transpose_kernel<true>, dim3(static_cast<unsigned>(g)), block, 0, stream,
-                                 src, lds, rows, cols, dst, dst_small, ldd);
+                                 src, lds, rows, cols, dst, dst_small, ldd, wl);
         return launch_kernel(dep, prep_transpose_kernel<false>, dim3(static_cast<unsigned>(g)), block, 0, stream, src,
-                             lds, rows, cols, dst, static_cast<float*>(nullptr), ldd);
+                             lds, rows, cols, dst, static_cast<float*>(nullptr), ldd, wl);
     } else if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && lds % 4 == 0 &&
                (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && ldd % 4 == 0 &&
                (dst_small == nullptr || (reinterpret_cast<uintptr_t>(dst_small) & 15u) == 0)) {
@@ -487,17 +497,17 @@ cudaError_t launch_prep(const float* src, int64_t lds, bool transposed, int64_t 
         if (g > cap) g = cap;
         if (dst_small)
             return launch_kernel(dep, prep_copy_vec_kernel<true>, dim3(static_cast<unsigned>(g)), dim3(256), 0,
-                                 stream, src, lds, rows, cols, dst, dst_small, ldd);
+                                 stream, src, lds, rows, cols, dst, dst_small, ldd, wl);
         return launch_kernel(dep, prep_copy_vec_kernel<false>, dim3(static_cast<unsigned>(g)), dim3(256), 0, stream,
-                             src, lds, rows, cols, dst, static_cast<float*>(nullptr), ldd);
+                             src, lds, rows, cols, dst, static_cast<float*>(nullptr), ldd, wl);
     }
     int sh = 8, by_rows = 0;
     const dim3 grid = sweep_grid(rows, cols, num_sms, &sh, &by_rows);
     if (dst_small)
         return launch_kernel(dep, prep_copy_kernel<true>, grid, dim3(256), 0, stream, src, lds, rows, cols, dst,
-                             dst_small, ldd, sh, by_rows);
+                             dst_small, ldd, sh, by_rows, wl);
     return launch_kernel(dep, prep_copy_kernel<false>, grid, dim3(256), 0, stream, src, lds, rows, cols, dst,
-                         static_cast<float*>(nullptr), ldd, sh, by_rows);
+                         static_cast<float*>(nullptr), ldd, sh, by_rows, wl);
 }
 
 cudaError_t launch_splitk_reduce(const GemmParams& p, int num_sms, cudaStream_t stream) {
