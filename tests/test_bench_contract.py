@@ -150,3 +150,23 @@ def test_bench_figures_and_config_helpers():
     assert cfg["l2"].startswith("inputs larger than L2") and cfg["parallelism"] == "single GPU"
     assert bench.make_config("square8192", bench.WORKLOADS["square8192"][1], ["ffma"], 4)["parallelism"] == "replicas"
     assert set(bench.SWEEP) <= set(synth.config_problems())
+
+
+def test_roofline_traffic_comes_only_from_a_matching_profile():
+    """roofline.traffic is read from the committed summary of the dominant kernel
+    only while the kernel source hash and the tile shape the planner picks both
+    match the ones the capture was taken on; otherwise it is null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import hashlib
+    text = open(os.path.join(ROOT, "profiles", "ffma_square8192.md")).read()
+    fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line and not line.startswith("#"))
+    tile = fields["tile"].strip()
+    want = int(fields["traffic_bytes_per_launch"].strip())
+    src = os.path.join(ROOT, "precision_gemm_gb300", "csrc", "ffma_kernel.cu")
+    current = hashlib.sha256(open(src, "rb").read()).hexdigest() == fields["source_sha256"].strip()
+    got = bench.read_traffic("ffma", "ffma", tile, "square8192")
+    assert got == (want if current else None)
+    other = "128x128" if tile != "128x128" else "128x64"
+    assert bench.read_traffic("ffma", "ffma", other, "square8192") is None
+    assert bench.read_traffic("ffma", "ffma", tile, "no_such_workload") is None
